@@ -1,0 +1,245 @@
+"""Python binding of libarnorm.so: fused AllReduce + residual-add + RMSNorm.
+
+Argument marshalling only.  Every step of the computation runs in the CUDA
+kernels of libarnorm.so (the C ABI declared in include/ar_rmsnorm.h); this
+module checks tensor shapes, dtypes and devices, turns tensors into raw
+device pointers and passes the current CUDA stream.  There is no CPU or
+PyTorch fallback: if the library is missing, importing ``lib()`` raises.
+
+Names follow the C ABI:
+
+    ar_rmsnorm(partials, residual, weight, eps, out=None, residual_out=None,
+               mode=AR_MODE_AUTO, stream=None) -> (out, residual_out)
+    ar_rmsnorm_ex(..., sum_out=None, cluster=0, vpt=0)
+    ar_reduce_scatter_flat(partials, temp, stream=None)
+    ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None)
+    ar_reserve_workspace(max_elems, device) / ar_release_workspace(device)
+    ar_workspace_elems(device), ar_select_mode(n, m, H),
+    ar_get_plan(n, m, H, mode, sm_count=0), ar_strerror(status), ar_version()
+"""
+import ctypes
+import os
+
+AR_OK = 0
+AR_ERR_ARG = 1
+AR_ERR_ALIGN = 2
+AR_ERR_ALIAS = 3
+AR_ERR_WORKSPACE = 4
+AR_ERR_CUDA = 5
+AR_ERR_TIMEOUT = 6
+AR_ERR_UNSUPPORTED = 7
+
+AR_MODE_AUTO = 0
+AR_MODE_ONE_STAGE = 1
+AR_MODE_TWO_STAGE = 2
+MODES = {"auto": AR_MODE_AUTO, "one_stage": AR_MODE_ONE_STAGE, "two_stage": AR_MODE_TWO_STAGE}
+
+AR_MAX_RANKS = 16
+AR_MAX_HIDDEN = 131072
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libarnorm.so")
+
+
+class ArError(RuntimeError):
+    def __init__(self, status, what):
+        self.status = status
+        super().__init__(f"{what}: status {status} ({_strerror(status)})")
+
+
+class ar_plan_t(ctypes.Structure):
+    _fields_ = [("mode", ctypes.c_int), ("cluster", ctypes.c_int), ("vpt", ctypes.c_int),
+                ("threads", ctypes.c_int), ("ctas", ctypes.c_int64), ("launches", ctypes.c_int)]
+
+
+_lib = None
+
+_VP = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_SIGS = {
+    "ar_rmsnorm": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP, ctypes.c_float,
+                                  _I64, _I64, _VP, _VP, ctypes.c_int, _VP]),
+    "ar_rmsnorm_ex": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP, ctypes.c_float,
+                                     _I64, _I64, _VP, _VP, ctypes.c_int, _VP, _VP,
+                                     ctypes.POINTER(ar_plan_t)]),
+    "ar_get_plan": (ctypes.c_int, [ctypes.c_int, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                   ctypes.POINTER(ar_plan_t)]),
+    "ar_reduce_scatter_flat": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _I64, _VP, _VP]),
+    "ar_load_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_float, _I64, _I64, _VP, _VP, _VP]),
+    "ar_reserve_workspace": (ctypes.c_int, [_I64, ctypes.c_int]),
+    "ar_release_workspace": (ctypes.c_int, [ctypes.c_int]),
+    "ar_workspace_elems": (_I64, [ctypes.c_int]),
+    "ar_select_mode": (ctypes.c_int, [ctypes.c_int, _I64, _I64]),
+    "ar_strerror": (ctypes.c_char_p, [ctypes.c_int]),
+    "ar_version": (ctypes.c_int, []),
+}
+
+
+def lib():
+    """The loaded libarnorm.so (ctypes), with argument types set."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is not built: run `python -c \"import __graft_entry__ as g; g.build()\"`"
+                " (the CUDA library is required; there is no fallback)")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _strerror(status):
+    try:
+        return lib().ar_strerror(int(status)).decode()
+    except Exception:  # pragma: no cover - only while the library is unavailable
+        return "unknown"
+
+
+def _check(status, what):
+    if status != AR_OK:
+        raise ArError(status, what)
+
+
+def _stream_ptr(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return _VP(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _ptr(t):
+    return _VP(t.data_ptr())
+
+
+def _check_tensor(t, name, shape, device):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if not t.is_cuda or (device is not None and t.device != device):
+        raise ValueError(f"{name} must be on {device or 'a CUDA device'}, got {t.device}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _prepare(partials, residual, weight, out, residual_out):
+    import torch
+    if len(partials) < 1:
+        raise ValueError("need at least one partial")
+    if residual.dim() != 2:
+        raise ValueError("residual must be [m, H]")
+    m, H = residual.shape
+    dev = residual.device
+    _check_tensor(residual, "residual", (m, H), None)
+    for k, p in enumerate(partials):
+        _check_tensor(p, f"partials[{k}]", (m, H), dev)
+    _check_tensor(weight, "weight", (H,), dev)
+    if out is None:
+        out = torch.empty_like(residual)
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    _check_tensor(out, "out", (m, H), dev)
+    _check_tensor(residual_out, "residual_out", (m, H), dev)
+    arr = (_VP * len(partials))(*[p.data_ptr() for p in partials])
+    return m, H, dev, out, residual_out, arr
+
+
+def ar_rmsnorm(partials, residual, weight, eps, out=None, residual_out=None,
+               mode=AR_MODE_AUTO, stream=None):
+    """Fused epilogue on the current (or given) stream; returns (out, residual_out).
+
+    partials: sequence of n bf16 [m, H] CUDA tensors, rank order = reduce order.
+    mode: AR_MODE_AUTO / AR_MODE_ONE_STAGE / AR_MODE_TWO_STAGE or "auto" /
+    "one_stage" / "two_stage".
+    """
+    mode = MODES.get(mode, mode)
+    m, H, dev, out, residual_out, arr = _prepare(partials, residual, weight, out, residual_out)
+    st = lib().ar_rmsnorm(arr, len(partials), _ptr(residual), _ptr(weight), float(eps), m, H,
+                          _ptr(out), _ptr(residual_out), int(mode), _stream_ptr(stream, dev))
+    _check(st, "ar_rmsnorm")
+    return out, residual_out
+
+
+def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
+                  mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0):
+    """ar_rmsnorm plus the reduced sum (fp32 [m, H] ``sum_out``) and a forced
+    launch shape (``cluster`` CTAs per row, ``vpt`` packs per thread; 0 =
+    library's choice).  Returns (out, residual_out, sum_out)."""
+    import torch
+    mode = MODES.get(mode, mode)
+    m, H, dev, out, residual_out, arr = _prepare(partials, residual, weight, out, residual_out)
+    if sum_out is not None:
+        if sum_out.dtype != torch.float32 or tuple(sum_out.shape) != (m, H) or \
+                not sum_out.is_contiguous() or sum_out.device != dev:
+            raise ValueError("sum_out must be a contiguous float32 [m, H] tensor on the inputs' device")
+    plan = None
+    if cluster or vpt:
+        plan = ctypes.pointer(ar_plan_t(0, int(cluster), int(vpt), 0, 0, 0))
+    st = lib().ar_rmsnorm_ex(arr, len(partials), _ptr(residual), _ptr(weight), float(eps), m, H,
+                             _ptr(out), _ptr(residual_out), int(mode), _stream_ptr(stream, dev),
+                             _VP(sum_out.data_ptr()) if sum_out is not None else None, plan)
+    _check(st, "ar_rmsnorm_ex")
+    return out, residual_out, sum_out
+
+
+def ar_reduce_scatter_flat(partials, temp, stream=None):
+    """Stage 1 alone: temp = bf16(rank-order fp32 sum of the partials)."""
+    count = temp.numel()
+    for k, p in enumerate(partials):
+        _check_tensor(p, f"partials[{k}]", tuple(temp.shape), temp.device)
+    _check_tensor(temp, "temp", tuple(temp.shape), temp.device)
+    arr = (_VP * len(partials))(*[p.data_ptr() for p in partials])
+    st = lib().ar_reduce_scatter_flat(arr, len(partials), count, _ptr(temp),
+                                      _stream_ptr(stream, temp.device))
+    _check(st, "ar_reduce_scatter_flat")
+    return temp
+
+
+def ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None, stream=None):
+    """Stage 2 alone: residual add and RMSNorm of an already reduced ``temp``."""
+    m, H, dev, out, residual_out, _ = _prepare([temp], residual, weight, out, residual_out)
+    st = lib().ar_load_rmsnorm(_ptr(temp), _ptr(residual), _ptr(weight), float(eps), m, H,
+                               _ptr(out), _ptr(residual_out), _stream_ptr(stream, dev))
+    _check(st, "ar_load_rmsnorm")
+    return out, residual_out
+
+
+def ar_reserve_workspace(max_elems, device=0):
+    _check(lib().ar_reserve_workspace(int(max_elems), int(device)), "ar_reserve_workspace")
+
+
+def ar_release_workspace(device=0):
+    _check(lib().ar_release_workspace(int(device)), "ar_release_workspace")
+
+
+def ar_workspace_elems(device=0):
+    return int(lib().ar_workspace_elems(int(device)))
+
+
+def ar_select_mode(n, m, H):
+    r = lib().ar_select_mode(int(n), int(m), int(H))
+    if r < 0:
+        raise ArError(-r, "ar_select_mode")
+    return r
+
+
+def ar_get_plan(n, m, H, mode=AR_MODE_AUTO, sm_count=0):
+    """The launch plan as a dict (pure host logic when sm_count > 0)."""
+    p = ar_plan_t()
+    _check(lib().ar_get_plan(int(n), int(m), int(H), int(MODES.get(mode, mode)), int(sm_count),
+                             ctypes.byref(p)), "ar_get_plan")
+    return {f: getattr(p, f) for f, _ in ar_plan_t._fields_}
+
+
+def ar_strerror(status):
+    return _strerror(status)
+
+
+def ar_version():
+    return int(lib().ar_version())

@@ -1,0 +1,431 @@
+// C ABI of libarnorm.so: argument checks, the one-/two-stage choice, launch
+// planning, the two-stage workspace and the launches.  Host code only.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "epilogue.cuh"
+
+namespace arn {
+
+EpilogueKernel epilogue_kernel_group0(int n, int vpt_log2);
+EpilogueKernel epilogue_kernel_group1(int n, int vpt_log2);
+EpilogueKernel epilogue_kernel_group2(int n, int vpt_log2);
+EpilogueKernel epilogue_kernel_group3(int n, int vpt_log2);
+cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream);
+
+static int vpt_log2(int vpt) { return vpt == 1 ? 0 : vpt == 2 ? 1 : vpt == 4 ? 2 : vpt == 8 ? 3 : -1; }
+
+EpilogueKernel epilogue_kernel(int n, int vpt) {
+  const int l = vpt_log2(vpt);
+  if (n < 1 || n > AR_MAX_RANKS || l < 0) return nullptr;
+  switch ((n - 1) / 4) {
+    case 0: return epilogue_kernel_group0(n, l);
+    case 1: return epilogue_kernel_group1(n, l);
+    case 2: return epilogue_kernel_group2(n, l);
+    default: return epilogue_kernel_group3(n, l);
+  }
+}
+
+// ---------------------------------------------------------------- per-device state
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+  bool ready = false;        // attributes read and kernel attributes set
+  int sms = 0;
+  void *workspace = nullptr; // two-stage bf16 temporary
+  int64_t workspace_elems = 0;
+};
+
+static std::mutex g_mu;
+static DeviceState g_dev[kMaxDevices];
+
+// Make the current device ready (SM count, kernel attributes); returns its
+// state or null.  Must run outside graph capture the first time.
+static DeviceState *current_device(int *status) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    *status = AR_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      *status = AR_ERR_CUDA;
+      return nullptr;
+    }
+    // Rows split over up to 16 CTAs need the non-portable cluster size.
+    for (int n = 1; n <= AR_MAX_RANKS; ++n)
+      for (int vpt = 1; vpt <= 8; vpt *= 2) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(epilogue_kernel(n, vpt)),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+          cudaGetLastError();
+          *status = AR_ERR_CUDA;
+          return nullptr;
+        }
+      }
+    d.ready = true;
+  }
+  *status = AR_OK;
+  return &d;
+}
+
+// ---------------------------------------------------------------- checks
+
+static bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+
+static bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
+
+static Range range_of(const void *p, int64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+
+static int check_shape(int n, int64_t m, int64_t H, float eps) {
+  if (n < 1 || n > AR_MAX_RANKS || m < 0 || H <= 0) return AR_ERR_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return AR_ERR_ARG;
+  if (H % kPackElems != 0) return AR_ERR_ALIGN;
+  if (H > AR_MAX_HIDDEN) return AR_ERR_UNSUPPORTED;
+  if (m > (int64_t{1} << 40) / H) return AR_ERR_UNSUPPORTED;  // keeps every byte count in range
+  return AR_OK;
+}
+
+// Pointers of a full epilogue call: null, alignment, then overlaps.
+static int check_buffers(const void *const *partials, int n, const void *residual,
+                         const void *weight, int64_t m, int64_t H, const void *out,
+                         const void *residual_out, const void *sum_out) {
+  if (!partials || !residual || !weight || !out || !residual_out) return AR_ERR_ARG;
+  for (int k = 0; k < n; ++k)
+    if (!partials[k]) return AR_ERR_ARG;
+  for (int k = 0; k < n; ++k)
+    if (!aligned16(partials[k])) return AR_ERR_ALIGN;
+  if (!aligned16(residual) || !aligned16(weight) || !aligned16(out) || !aligned16(residual_out) ||
+      (sum_out && !aligned16(sum_out)))
+    return AR_ERR_ALIGN;
+  const int64_t bytes = m * H * 2;
+  const Range o = range_of(out, bytes), ro = range_of(residual_out, bytes);
+  const Range res = range_of(residual, bytes), w = range_of(weight, H * 2);
+  if (overlap(o, ro) || overlap(o, res) || overlap(o, w)) return AR_ERR_ALIAS;
+  if (overlap(ro, w)) return AR_ERR_ALIAS;
+  if (overlap(ro, res) && residual_out != residual) return AR_ERR_ALIAS;
+  for (int k = 0; k < n; ++k) {
+    const Range p = range_of(partials[k], bytes);
+    if (overlap(p, o) || overlap(p, ro)) return AR_ERR_ALIAS;
+  }
+  if (sum_out) {
+    const Range s = range_of(sum_out, m * H * 4);
+    if (overlap(s, o) || overlap(s, ro) || overlap(s, res) || overlap(s, w)) return AR_ERR_ALIAS;
+    for (int k = 0; k < n; ++k)
+      if (overlap(s, range_of(partials[k], bytes))) return AR_ERR_ALIAS;
+  }
+  return AR_OK;
+}
+
+// ---------------------------------------------------------------- policy
+
+// One-stage up to this many rows, two-stage above (0 = never two-stage).
+// Set from the GB300 sweep of both paths (see the bench's sweep mode).
+static int64_t one_stage_max_rows(int n, int64_t H) {
+  (void)n;
+  (void)H;
+  return INT64_MAX;
+}
+
+static int select_mode(int n, int64_t m, int64_t H) {
+  return m <= one_stage_max_rows(n, H) ? AR_MODE_ONE_STAGE : AR_MODE_TWO_STAGE;
+}
+
+// Launch shape of the epilogue kernel for m rows of P packs with n inputs.
+//  * cluster S: the fewest CTAs per row that hold a row in registers
+//    (<= 1024 packs per CTA), then doubled while the grid (m * S) does not
+//    yet give every SM a CTA and each CTA keeps >= 32 packs.
+//  * vpt: when rows alone fill the GPU (m >= 2 * SMs), the fewest packs per
+//    thread that keep a CTA at <= 256 threads (several CTAs per SM);
+//    otherwise 1 pack per thread, i.e. the most loads in flight at once
+//    for a short grid.  Either way a CTA stays within 1024 / vpt threads.
+static void plan_epilogue(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
+                          ar_plan_t *pl) {
+  int S = 1;
+  while (S < kMaxClusterCtas && (P + S - 1) / S > kMaxPacksPerCta) S *= 2;
+  while (S < kMaxClusterCtas && m * S < sms && (P + 2 * S - 1) / (2 * S) >= 32) S *= 2;
+  if (force_cluster > 0) S = force_cluster;
+  const int64_t per_cta = (P + S - 1) / S;
+  int vpt = 1;
+  if (m >= 2 * static_cast<int64_t>(sms))
+    while (vpt < 8 && (per_cta + vpt - 1) / vpt > 256) vpt *= 2;
+  while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
+  if (force_vpt > 0) vpt = force_vpt;
+  int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
+  threads = (threads + 31) / 32 * 32;
+  pl->cluster = S;
+  pl->vpt = vpt;
+  pl->threads = threads;
+  pl->ctas = m * S;
+}
+
+static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, const ar_plan_t *force,
+                     ar_plan_t *pl) {
+  if (mode != AR_MODE_AUTO && mode != AR_MODE_ONE_STAGE && mode != AR_MODE_TWO_STAGE)
+    return AR_ERR_ARG;
+  std::memset(pl, 0, sizeof *pl);
+  pl->mode = mode == AR_MODE_AUTO ? select_mode(n, m, H) : mode;
+  int fc = 0, fv = 0;
+  if (force) {
+    fc = force->cluster;
+    fv = force->vpt;
+    if (fc != 0 && fc != 1 && fc != 2 && fc != 4 && fc != 8 && fc != 16) return AR_ERR_ARG;
+    if (fv != 0 && vpt_log2(fv) < 0) return AR_ERR_ARG;
+  }
+  const int64_t P = H / kPackElems;
+  plan_epilogue(m, P, sms, fc, fv, pl);
+  const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;
+  if (per_cta > static_cast<int64_t>(pl->vpt) * (1024 / pl->vpt)) return AR_ERR_ARG;  // forced shape too small
+  if (pl->ctas > INT32_MAX) return AR_ERR_UNSUPPORTED;
+  pl->launches = pl->mode == AR_MODE_TWO_STAGE ? 2 : 1;
+  return AR_OK;
+}
+
+static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t &pl,
+                                   cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (pl.cluster > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt), a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n,
+                               const void *residual, const void *weight, float eps, int64_t m,
+                               int64_t H, void *out, void *residual_out, float *sum_out,
+                               const ar_plan_t &pl) {
+  std::memset(a, 0, sizeof *a);
+  for (int k = 0; k < n; ++k) a->p[k] = static_cast<const uint4 *>(inputs[k]);
+  a->res = static_cast<const uint4 *>(residual);
+  a->w = static_cast<const uint4 *>(weight);
+  a->out = static_cast<uint4 *>(out);
+  a->rout = static_cast<uint4 *>(residual_out);
+  a->sum = reinterpret_cast<float4 *>(sum_out);
+  a->m = m;
+  a->P = static_cast<int>(H / kPackElems);
+  a->per_cta = static_cast<int>((a->P + pl.cluster - 1) / pl.cluster);
+  a->H = static_cast<float>(H);
+  a->eps = eps;
+}
+
+static int run(const void *const *partials, int n, const void *residual, const void *weight,
+               float eps, int64_t m, int64_t H, void *out, void *residual_out, int mode,
+               void *stream, float *sum_out, const ar_plan_t *force) {
+  int st = check_shape(n, m, H, eps);
+  if (st != AR_OK) return st;
+  if (mode != AR_MODE_AUTO && mode != AR_MODE_ONE_STAGE && mode != AR_MODE_TWO_STAGE)
+    return AR_ERR_ARG;
+  if (m == 0) return AR_OK;  // nothing is read or written; pointers may be null
+  st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, sum_out);
+  if (st != AR_OK) return st;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  ar_plan_t pl;
+  st = make_plan(n, m, H, mode, d->sms, force, &pl);
+  if (st != AR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  EpilogueArgs a;
+  if (pl.mode == AR_MODE_ONE_STAGE) {
+    fill_epilogue_args(&a, partials, n, residual, weight, eps, m, H, out, residual_out, sum_out, pl);
+    return launch_epilogue(a, n, pl, s) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+  }
+  // two-stage: stage 1 into the workspace, stage 2 from it
+  void *ws;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->workspace == nullptr || d->workspace_elems < m * H) return AR_ERR_WORKSPACE;
+    ws = d->workspace;
+  }
+  const Range wr = range_of(ws, m * H * 2);
+  const int64_t bytes = m * H * 2;
+  if (overlap(wr, range_of(out, bytes)) || overlap(wr, range_of(residual_out, bytes)) ||
+      overlap(wr, range_of(residual, bytes)) || overlap(wr, range_of(weight, H * 2)) ||
+      (sum_out && overlap(wr, range_of(sum_out, m * H * 4))))
+    return AR_ERR_ALIAS;
+  for (int k = 0; k < n; ++k)
+    if (overlap(wr, range_of(partials[k], bytes))) return AR_ERR_ALIAS;
+  ReduceArgs ra;
+  std::memset(&ra, 0, sizeof ra);
+  for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
+  ra.temp = static_cast<uint4 *>(ws);
+  ra.npacks = m * H / kPackElems;
+  if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
+  const void *temp_in[1] = {ws};
+  fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, sum_out, pl);
+  return launch_epilogue(a, 1, pl, s) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+}
+
+}  // namespace arn
+
+using namespace arn;
+
+extern "C" {
+
+int ar_rmsnorm(const void *const *partials, int n, const void *residual, const void *weight,
+               float eps, int64_t m, int64_t H, void *out, void *residual_out, int mode,
+               void *stream) {
+  return run(partials, n, residual, weight, eps, m, H, out, residual_out, mode, stream, nullptr,
+             nullptr);
+}
+
+int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual, const void *weight,
+                  float eps, int64_t m, int64_t H, void *out, void *residual_out, int mode,
+                  void *stream, float *sum_out, const ar_plan_t *plan) {
+  return run(partials, n, residual, weight, eps, m, H, out, residual_out, mode, stream, sum_out,
+             plan);
+}
+
+int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count, ar_plan_t *plan) {
+  if (!plan) return AR_ERR_ARG;
+  int st = check_shape(n, m, H, 0.f);
+  if (st != AR_OK) return st;
+  if (sm_count <= 0) {
+    DeviceState *d = current_device(&st);
+    if (!d) return st;
+    sm_count = d->sms;
+  }
+  return make_plan(n, m, H, mode, sm_count, nullptr, plan);
+}
+
+int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count, void *temp,
+                           void *stream) {
+  if (n < 1 || n > AR_MAX_RANKS || count < 0) return AR_ERR_ARG;
+  if (count % kPackElems != 0) return AR_ERR_ALIGN;
+  if (count > (int64_t{1} << 40)) return AR_ERR_UNSUPPORTED;
+  if (count == 0) return AR_OK;  // nothing is read or written; pointers may be null
+  if (!partials || !temp) return AR_ERR_ARG;
+  for (int k = 0; k < n; ++k)
+    if (!partials[k]) return AR_ERR_ARG;
+  if (!aligned16(temp)) return AR_ERR_ALIGN;
+  for (int k = 0; k < n; ++k)
+    if (!aligned16(partials[k])) return AR_ERR_ALIGN;
+  for (int k = 0; k < n; ++k)
+    if (overlap(range_of(partials[k], count * 2), range_of(temp, count * 2))) return AR_ERR_ALIAS;
+  int st;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  ReduceArgs ra;
+  std::memset(&ra, 0, sizeof ra);
+  for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
+  ra.temp = static_cast<uint4 *>(temp);
+  ra.npacks = count / kPackElems;
+  return launch_reduce_flat(ra, n, d->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? AR_OK
+             : AR_ERR_CUDA;
+}
+
+int ar_load_rmsnorm(const void *temp, const void *residual, const void *weight, float eps,
+                    int64_t m, int64_t H, void *out, void *residual_out, void *stream) {
+  const void *inputs[1] = {temp};
+  return run(inputs, 1, residual, weight, eps, m, H, out, residual_out, AR_MODE_ONE_STAGE, stream,
+             nullptr, nullptr);
+}
+
+int ar_reserve_workspace(int64_t max_elems, int device) {
+  if (max_elems < 0 || device < 0 || device >= kMaxDevices) return AR_ERR_ARG;
+  if (max_elems > (int64_t{1} << 40)) return AR_ERR_UNSUPPORTED;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  if (cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  int st;
+  DeviceState *d = current_device(&st);
+  if (d) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->workspace_elems < max_elems) {
+      if (d->workspace) {
+        cudaDeviceSynchronize();
+        cudaFree(d->workspace);
+        d->workspace = nullptr;
+        d->workspace_elems = 0;
+      }
+      const int64_t elems = (max_elems + 7) / 8 * 8;
+      if (cudaMalloc(&d->workspace, static_cast<size_t>(elems) * 2) != cudaSuccess) {
+        cudaGetLastError();
+        d->workspace = nullptr;
+        st = AR_ERR_CUDA;
+      } else {
+        d->workspace_elems = elems;
+      }
+    }
+  }
+  cudaSetDevice(prev);
+  return st;
+}
+
+int ar_release_workspace(int device) {
+  if (device < 0 || device >= kMaxDevices) return AR_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &d = g_dev[device];
+  if (!d.workspace) return AR_OK;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  cudaDeviceSynchronize();
+  const cudaError_t e = cudaFree(d.workspace);
+  d.workspace = nullptr;
+  d.workspace_elems = 0;
+  cudaSetDevice(prev);
+  return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+}
+
+int64_t ar_workspace_elems(int device) {
+  if (device < 0 || device >= kMaxDevices) return -1;
+  std::lock_guard<std::mutex> lock(g_mu);
+  return g_dev[device].workspace_elems;
+}
+
+int ar_select_mode(int n, int64_t m, int64_t H) {
+  if (n < 1 || n > AR_MAX_RANKS || m < 0 || H <= 0) return -AR_ERR_ARG;
+  return select_mode(n, m, H);
+}
+
+const char *ar_strerror(int status) {
+  switch (status) {
+    case AR_OK: return "success";
+    case AR_ERR_ARG: return "invalid argument (n, m, H, eps, mode or a null pointer)";
+    case AR_ERR_ALIGN: return "misaligned: pointers must be 16-byte aligned and H a multiple of 8";
+    case AR_ERR_ALIAS: return "overlapping buffers (only residual_out == residual may alias)";
+    case AR_ERR_WORKSPACE: return "two-stage workspace missing or too small: call ar_reserve_workspace";
+    case AR_ERR_CUDA: return "CUDA runtime error or launch failure";
+    case AR_ERR_TIMEOUT: return "a bounded device-side wait timed out";
+    case AR_ERR_UNSUPPORTED: return "unsupported size (H above AR_MAX_HIDDEN or too many rows)";
+    default: return "unknown status";
+  }
+}
+
+int ar_version(void) { return 100; }
+
+}  // extern "C"

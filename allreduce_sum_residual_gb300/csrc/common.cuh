@@ -1,0 +1,131 @@
+// Device-side building blocks shared by the ar_rmsnorm kernels (sm_103a).
+//
+// A "pack" is 16 bytes = 8 bf16: the unit every thread loads and stores, so
+// that a warp moves 512 contiguous bytes per instruction.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ar_rmsnorm.h"
+
+namespace arn {
+
+constexpr int kPackElems = 8;            // bf16 per 16-byte pack
+constexpr int kMaxClusterCtas = 16;      // widest row split (non-portable cluster)
+constexpr int kMaxPacksPerCta = 1024;    // 8192 columns held in registers per CTA
+
+// Kernel parameters of the fused epilogue (one-stage, and stage 2 with n = 1).
+struct EpilogueArgs {
+  const uint4 *p[AR_MAX_RANKS];  // partial k, [m, H/8] packs, rank order
+  const uint4 *res;              // residual [m, H/8]
+  const uint4 *w;                // weight [H/8]
+  uint4 *out;                    // [m, H/8]
+  uint4 *rout;                   // residual_out [m, H/8]
+  float4 *sum;                   // optional fp32 sum [m, H/4] float4s, or null
+  int64_t m;                     // rows
+  int P;                         // packs per row = H / 8
+  int per_cta;                   // packs of a row one CTA covers
+  float H;                       // columns, as the divisor of the mean
+  float eps;
+};
+
+// Kernel parameters of stage 1 (flat reduce of every pack across ranks).
+struct ReduceArgs {
+  const uint4 *p[AR_MAX_RANKS];
+  uint4 *temp;
+  int64_t npacks;
+};
+
+// --- bf16 <-> fp32 ----------------------------------------------------------
+
+// Widen the 8 bf16 of a pack: a bf16 is the top half of an fp32.
+__device__ __forceinline__ void unpack8(const uint4 &v, float (&f)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+// Round 8 fp32 to bf16 (nearest even, one cvt.rn.bf16x2.f32 per pair).
+__device__ __forceinline__ uint4 pack8(const float (&f)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+    w[i] = *reinterpret_cast<uint32_t *>(&h);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// --- global memory ------------------------------------------------------------
+
+// Read-only 16-byte load through the non-coherent path; the data is never
+// written during the kernel, which lets the compiler hoist these freely.
+__device__ __forceinline__ uint4 ld_ro(const uint4 *p) { return __ldg(p); }
+
+// Streaming 16-byte store: the outputs are not re-read by this kernel.
+__device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
+// --- reductions -----------------------------------------------------------------
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Sum of `v` over the CTA, returned to every thread.  `scratch` holds 33
+// floats.  Butterfly within each warp, one slot per warp, then warp 0 folds
+// the slots (the square-sum order is not part of the bit-exact contract).
+__device__ __forceinline__ float block_sum(float v, float *scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = (blockDim.x + 31) >> 5;
+  v = warp_sum(v);
+  if (lane == 0) scratch[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    float t = lane < nwarps ? scratch[lane] : 0.f;
+    t = warp_sum(t);
+    if (lane == 0) scratch[32] = t;
+  }
+  __syncthreads();
+  return scratch[32];
+}
+
+// --- thread-block clusters --------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// Cluster-wide barrier; release/acquire order shared-memory writes before it
+// against distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float from the shared memory of CTA `rank` of this cluster, at the
+// address that `local` has in this CTA.
+__device__ __forceinline__ float ld_dsmem(const float *local, uint32_t rank) {
+  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+  return v;
+}
+
+}  // namespace arn

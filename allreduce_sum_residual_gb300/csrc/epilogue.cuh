@@ -1,0 +1,121 @@
+// The fused epilogue kernel: rank-order fp32 sum of n partials, residual
+// add, RMSNorm.  One-stage uses it with the n partials; stage 2 of the
+// two-stage path uses it with n = 1 and the bf16 temporary as the only
+// partial (ROCm/aiter #3817 "perf: optimize fused AllReduce + RMSNorm
+// (custom_all_reduce)", Technical Details: 1stage decode path, and 2stage
+// stage-2 local_device_load_rmsnorm).
+//
+// Work split.  A row of H columns is P = H/8 packs.  The CTAs of one
+// thread-block cluster (S = 1..16 CTAs, consecutive in x) share a row: CTA
+// rank q covers packs [q*per_cta, (q+1)*per_cta).  Thread t of a CTA covers
+// packs t, t+T, t+2T, ... (VPT of them), so each warp load is 512 contiguous
+// bytes.  Every partial element is owned by exactly one thread, which sums
+// it over the ranks in order: the sum does not depend on S, T or VPT.
+//
+// The square sum is reduced warp -> CTA -> cluster; the cluster step reads
+// each CTA's total from distributed shared memory in rank order, so every
+// CTA of a row derives the same scale.
+#pragma once
+
+#include "common.cuh"
+
+namespace arn {
+
+// acc = p_0 + p_1 + ... + p_{N-1} for one pack, in fp32, in rank order.
+// Used by every path, so one-stage, stage 1 and stage 2 share this exact
+// sequence of fp32 adds.
+template <int N>
+__device__ __forceinline__ void sum_pack_in_rank_order(const uint4 *const (&p)[AR_MAX_RANKS],
+                                                       int64_t idx, float (&acc)[8]) {
+  uint4 x[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) x[k] = ld_ro(p[k] + idx);
+  unpack8(x[0], acc);
+#pragma unroll
+  for (int k = 1; k < N; ++k) {
+    float t[8];
+    unpack8(x[k], t);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], t[e]);
+  }
+}
+
+template <int N, int VPT>
+__global__ void __launch_bounds__(1024 / VPT)
+k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
+  __shared__ float red[33];
+  __shared__ float cta_total;
+
+  const uint32_t S = cluster_nctarank();       // 1 unless launched as a cluster
+  const uint32_t q = cluster_ctarank();
+  const int64_t row = blockIdx.x / S;
+  const int c0 = static_cast<int>(q) * a.per_cta;
+  const int c1 = min(a.P, c0 + a.per_cta);
+  const int64_t base = row * static_cast<int64_t>(a.P);
+  const int T = blockDim.x;
+
+  // Loads first: n partials, the residual and the weight of every pack this
+  // thread owns.  Nothing is stored before the last load is issued.
+  float r[VPT][8];
+  uint4 wv[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
+    if (c < c1) {
+      float acc[8], rs[8];
+      sum_pack_in_rank_order<N>(a.p, base + c, acc);
+      unpack8(ld_ro(a.res + base + c), rs);
+      wv[v] = ld_ro(a.w + c);
+      if (a.sum != nullptr) {
+        a.sum[2 * (base + c)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        a.sum[2 * (base + c) + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[v][e] = __fadd_rn(acc[e], rs[e]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[v][e] = 0.f;
+      wv[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  // residual_out = bf16(r); square sum of this thread's r.
+  float ss = 0.f;
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
+    if (c < c1) st_stream(a.rout + base + c, pack8(r[v]));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(r[v][e], r[v][e], ss);
+  }
+
+  float total = block_sum(ss, red);
+  if (S > 1) {
+    if (threadIdx.x == 0) cta_total = total;
+    cluster_sync();
+    total = 0.f;
+    for (uint32_t k = 0; k < S; ++k) total += ld_dsmem(&cta_total, k);
+  }
+  const float inv = rsqrtf(total / a.H + a.eps);
+
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
+    if (c < c1) {
+      float w[8], y[8];
+      unpack8(wv[v], w);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = (r[v][e] * inv) * w[e];
+      st_stream(a.out + base + c, pack8(y));
+    }
+  }
+
+  // No CTA may leave while a peer can still read its cta_total.
+  if (S > 1) cluster_sync();
+}
+
+// Kernel pointer for (n, vpt); n in [1, AR_MAX_RANKS], vpt in {1, 2, 4, 8}.
+using EpilogueKernel = void (*)(EpilogueArgs);
+EpilogueKernel epilogue_kernel(int n, int vpt);
+
+}  // namespace arn

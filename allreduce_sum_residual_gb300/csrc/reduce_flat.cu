@@ -1,0 +1,64 @@
+// Stage 1 of the two-stage path: a flat reduce of every 16-byte pack across
+// the n ranks, rounded to bf16 into the temporary buffer.
+//
+// ROCm/aiter #3817 "perf: optimize fused AllReduce + RMSNorm
+// (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: each
+// thread reduces one pack across all input ranks in fp32, downcasts the sum
+// to bf16 and stores it; no shared memory and no block barrier; the rank
+// order ptrs[0..n-1] is kept.  Stage-1 launch config: 256-thread blocks.
+//
+// On one GPU the "scatter" has one destination (this GPU's temporary).  The
+// grid is a multiple of the SM count and strides over all packs; each step
+// of a thread handles U packs 256 apart, issuing all U*n loads before the
+// first add.
+#include "epilogue.cuh"
+
+namespace arn {
+
+constexpr int kReduceThreads = 256;
+
+template <int N, int U>
+__global__ void __launch_bounds__(kReduceThreads)
+k_reduce_flat(const __grid_constant__ ReduceArgs a) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads * U;
+  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kReduceThreads * U + threadIdx.x;
+       i0 < a.npacks; i0 += stride) {
+    float acc[U][8];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t idx = i0 + static_cast<int64_t>(u) * kReduceThreads;
+      if (idx < a.npacks) sum_pack_in_rank_order<N>(a.p, idx, acc[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int64_t idx = i0 + static_cast<int64_t>(u) * kReduceThreads;
+      if (idx < a.npacks) st_stream(a.temp + idx, pack8(acc[u]));
+    }
+  }
+}
+
+constexpr int kReduceUnroll = 2;
+
+using ReduceKernel = void (*)(ReduceArgs);
+
+static ReduceKernel reduce_kernel(int n) {
+#define ARN_R(N) &k_reduce_flat<N, kReduceUnroll>
+  static const ReduceKernel table[AR_MAX_RANKS] = {
+      ARN_R(1), ARN_R(2), ARN_R(3), ARN_R(4), ARN_R(5), ARN_R(6), ARN_R(7), ARN_R(8),
+      ARN_R(9), ARN_R(10), ARN_R(11), ARN_R(12), ARN_R(13), ARN_R(14), ARN_R(15), ARN_R(16)};
+#undef ARN_R
+  return table[n - 1];
+}
+
+// Launch stage 1 over `npacks` packs; `sms` is the device's SM count.
+cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream) {
+  const int64_t per_block = static_cast<int64_t>(kReduceThreads) * kReduceUnroll;
+  int64_t blocks = (a.npacks + per_block - 1) / per_block;
+  const int64_t cap = static_cast<int64_t>(sms) * (2048 / kReduceThreads);
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  reduce_kernel(n)<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace arn

@@ -1,0 +1,200 @@
+/*
+ * ar_rmsnorm — fused AllReduce + residual-add + RMSNorm for GB300 (sm_103a).
+ *
+ * C ABI of libarnorm.so.  Plain pointers and sizes only; no C++ or torch
+ * types cross this boundary, nothing throws or aborts across it.
+ *
+ * The operation (the epilogue of a tensor-parallel decoder layer):
+ *
+ *   for each row i < m and column j < H
+ *     s      = p_0[i,j] + p_1[i,j] + ... + p_{n-1}[i,j]   fp32, rank order
+ *     r      = s + residual[i,j]                           fp32
+ *     residual_out[i,j] = bf16(r)
+ *     out[i,j]          = bf16(r * rsqrt(mean_j(r^2) + eps) * weight[j])
+ *
+ * The n partials are the n ranks' buffers of an all-reduce; on one GPU they
+ * all live in this GPU's memory.  The sum is taken in fp32 strictly in the
+ * order partials[0], partials[1], ..., partials[n-1], so it is bit-exact and
+ * independent of the launch shape (ROCm/aiter #3817 "perf: optimize fused
+ * AllReduce + RMSNorm (custom_all_reduce)", Technical Details, 2stage,
+ * reduce-scatter: the reduce order over ptrs[0..ngpus-1] is kept).
+ *
+ * Two paths compute it:
+ *   one-stage  a single kernel, one pass over memory (same page, Technical
+ *              Details, 1stage: the decode path with a block reduce of the
+ *              square sum);
+ *   two-stage  stage 1 reduces every 16-byte pack across the ranks and
+ *              writes the sum, rounded to bf16, to a temporary buffer; stage
+ *              2 loads it, adds the residual and normalises (same page,
+ *              2stage: reduce-scatter, stage-1 launch config, stage-2
+ *              RMSNorm reduce).  Because of that rounding, two-stage results
+ *              are those of s' = bf16(s) in place of s.
+ *
+ * Data layout: every tensor is bf16, contiguous and row-major; partials,
+ * residual, out and residual_out are [m, H] and weight is [H]
+ * (contiguous bf16 (tokens, hidden) tensors with a bf16 weight, the scope
+ * validated in lightseekorg/tokenspeed #968 "perf(comm): add opt-in Triton
+ * AR+RMSNorm backend", Summary).
+ * Every pointer must be 16-byte aligned and H a multiple of 8 (one 16-byte
+ * pack = 8 bf16).
+ *
+ * Ownership: all tensors belong to the caller and live in device memory of
+ * the current device.  The library owns only the two-stage workspace, and
+ * only after ar_reserve_workspace.  The host array `partials` is read during
+ * the call only and may be freed when the call returns.
+ *
+ * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream).  No call that launches work synchronises the
+ * host or allocates, so the calls may be captured in a CUDA graph.  The
+ * first launching call on a device sets kernel attributes; make one call
+ * (or ar_reserve_workspace) before capturing.
+ *
+ * Aliasing: residual_out may equal residual (in place).  Any other overlap
+ * between out, residual_out, residual, the partials and the workspace is
+ * rejected with AR_ERR_ALIAS.
+ */
+#ifndef AR_RMSNORM_H
+#define AR_RMSNORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every call. */
+#define AR_OK              0  /* success; m == 0 (or count == 0) is a no-op that
+                                 checks only the sizes, pointers may be NULL    */
+#define AR_ERR_ARG         1  /* n outside [1, AR_MAX_RANKS], m < 0, H <= 0,
+                                 eps negative or not finite, NULL pointer,
+                                 unknown mode                                   */
+#define AR_ERR_ALIGN       2  /* a pointer not 16-byte aligned, or H % 8 != 0 */
+#define AR_ERR_ALIAS       3  /* overlapping buffers other than
+                                 residual_out == residual                       */
+#define AR_ERR_WORKSPACE   4  /* two-stage with m*H above the reserved
+                                 workspace of the current device               */
+#define AR_ERR_CUDA        5  /* a CUDA runtime call or a launch failed        */
+#define AR_ERR_TIMEOUT     6  /* a bounded device-side wait ran out            */
+#define AR_ERR_UNSUPPORTED 7  /* H above AR_MAX_HIDDEN                         */
+
+/* Modes. */
+#define AR_MODE_AUTO       0  /* pick by ar_select_mode(n, m, H)               */
+#define AR_MODE_ONE_STAGE  1
+#define AR_MODE_TWO_STAGE  2
+
+#define AR_MAX_RANKS  16      /* most partials one call reduces                */
+#define AR_MAX_HIDDEN 131072  /* largest H (16 CTAs x 8192 columns)            */
+
+/*
+ * The fused epilogue.
+ *   partials     host array of n device pointers, each [m, H] bf16; index
+ *                order is the reduce order.
+ *   n            number of partials (ranks), 1 .. AR_MAX_RANKS.
+ *   residual     [m, H] bf16, device.
+ *   weight       [H] bf16, device (the RMSNorm gain).
+ *   eps          added to mean(r^2) inside the square root; finite, >= 0.
+ *   m, H         rows (tokens) and hidden size.
+ *   out          [m, H] bf16, device: the normalised output.
+ *   residual_out [m, H] bf16, device: bf16(sum + residual); may be residual.
+ *   mode         AR_MODE_AUTO, AR_MODE_ONE_STAGE or AR_MODE_TWO_STAGE.
+ *   stream       cudaStream_t to launch on.
+ * Returns AR_OK or an AR_ERR_* code; on error nothing is launched.
+ */
+int ar_rmsnorm(const void *const *partials, int n, const void *residual,
+               const void *weight, float eps, int64_t m, int64_t H, void *out,
+               void *residual_out, int mode, void *stream);
+
+/*
+ * What one call launches: the path and the launch shape of the fused
+ * epilogue kernel (one-stage, or stage 2 of two-stage).
+ */
+typedef struct {
+  int mode;        /* AR_MODE_ONE_STAGE or AR_MODE_TWO_STAGE                  */
+  int cluster;     /* CTAs sharing one row (a thread-block cluster), 1..16    */
+  int vpt;         /* 16-byte packs per thread: 1, 2, 4 or 8                  */
+  int threads;     /* threads per CTA                                          */
+  int64_t ctas;    /* CTAs of the epilogue kernel (m * cluster)               */
+  int launches;    /* kernels one call launches (1 or 2)                      */
+} ar_plan_t;
+
+/*
+ * The plan ar_rmsnorm would follow for (n, m, H, mode) on a GPU with
+ * `sm_count` SMs (0: ask the current device).  Pure host logic when
+ * sm_count > 0.  Returns AR_OK or AR_ERR_ARG / AR_ERR_ALIGN /
+ * AR_ERR_UNSUPPORTED as ar_rmsnorm would.
+ */
+int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count,
+                ar_plan_t *plan);
+
+/*
+ * As ar_rmsnorm, with two additions for testing and tuning:
+ *   sum_out  [m, H] fp32 device buffer (16-byte aligned) that receives the
+ *            reduced sum feeding the residual add: the fp32 accumulator for
+ *            one-stage, the widened bf16 temporary for two-stage.  NULL to
+ *            skip.  Costs 4*m*H extra bytes of writes.
+ *   plan     NULL for the library's choice, else its `cluster` and `vpt`
+ *            fields force the launch shape of the epilogue kernel (0 =
+ *            library's choice; cluster in {1,2,4,8,16}, vpt in {1,2,4,8},
+ *            and a CTA may cover at most 1024 packs, else AR_ERR_ARG).  The
+ *            other fields are ignored; `mode` still picks the path.  The
+ *            results do not depend on the launch shape.
+ */
+int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
+                  const void *weight, float eps, int64_t m, int64_t H,
+                  void *out, void *residual_out, int mode, void *stream,
+                  float *sum_out, const ar_plan_t *plan);
+
+/*
+ * Stage 1 alone: temp[e] = bf16(p_0[e] + ... + p_{n-1}[e]) for e < count,
+ * fp32 rank-order sum, one 16-byte pack per thread step, no shared memory
+ * and no block barrier (ROCm/aiter #3817, Technical Details, 2stage,
+ * reduce-scatter).  count must be a multiple of 8; temp is caller-owned
+ * device memory of count bf16 and must not overlap a partial.
+ */
+int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count,
+                           void *temp, void *stream);
+
+/*
+ * Stage 2 alone: the epilogue with a single, already reduced input `temp`
+ * ([m, H] bf16): r = temp + residual, then RMSNorm (ROCm/aiter #3817,
+ * Technical Details, 2stage, stage-2 RMSNorm reduce:
+ * local_device_load_rmsnorm).  Arguments as in ar_rmsnorm.
+ */
+int ar_load_rmsnorm(const void *temp, const void *residual, const void *weight,
+                    float eps, int64_t m, int64_t H, void *out,
+                    void *residual_out, void *stream);
+
+/*
+ * Reserve the two-stage workspace (max_elems bf16 elements, i.e. the largest
+ * m*H the two-stage path will see) on `device`.  Allocates with cudaMalloc,
+ * so call it before any graph capture.  Growing replaces the old buffer
+ * (after a device synchronisation); a smaller request keeps the current one.
+ */
+int ar_reserve_workspace(int64_t max_elems, int device);
+
+/* Free the workspace of `device` (synchronises the device first). */
+int ar_release_workspace(int device);
+
+/* Elements (bf16) of workspace currently reserved on `device`, or -1. */
+int64_t ar_workspace_elems(int device);
+
+/*
+ * The mode AR_MODE_AUTO picks for (n, m, H): AR_MODE_ONE_STAGE or
+ * AR_MODE_TWO_STAGE, from a threshold table measured on GB300 (the pages'
+ * own rule, one-stage for m <= 32 at 4 ranks and m <= 16 at 8, was set on
+ * MI355X: ROCm/aiter #3817, Test Results).  Pure host logic; needs no GPU.
+ * Returns -AR_ERR_ARG for n outside [1, AR_MAX_RANKS], m < 0 or H <= 0.
+ */
+int ar_select_mode(int n, int64_t m, int64_t H);
+
+/* A short English description of a status code (static storage). */
+const char *ar_strerror(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int ar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AR_RMSNORM_H */

@@ -27,3 +27,12 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def arlib():
+    """libarnorm.so, built in tree if needed (nvcc cross-compiles on the CPU)."""
+    from allreduce_sum_residual_gb300 import _build
+    _build.build()
+    import allreduce_sum_residual_gb300 as arn
+    return arn

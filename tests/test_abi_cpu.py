@@ -1,0 +1,162 @@
+"""The C ABI without a GPU: it loads, exports every declared symbol, checks
+its arguments before touching CUDA, and plans launches by pure host logic."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, ARG, ALIGN, ALIAS, WORKSPACE, CUDA, TIMEOUT, UNSUPPORTED = range(8)
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names |= set(re.findall(r"^[A-Za-z_][\w\s\*]*?\b(ar_\w+)\s*\(", src, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("ar_rmsnorm", "ar_rmsnorm_ex", "ar_reduce_scatter_flat", "ar_load_rmsnorm",
+                 "ar_reserve_workspace", "ar_release_workspace", "ar_select_mode",
+                 "ar_get_plan", "ar_strerror"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(arlib):
+    so = ctypes.CDLL(arlib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, f"declared but not exported: {missing}"
+
+
+def test_version_and_strerror(arlib):
+    assert arlib.ar_version() >= 100
+    msgs = {arlib.ar_strerror(s) for s in range(8)}
+    assert len(msgs) == 8 and all(msgs)
+    assert arlib.ar_strerror(99) == "unknown status"
+
+
+# Fake, never dereferenced device addresses: validation rejects these calls
+# (or returns early for m = 0) before any CUDA call.
+BASE = 0x7F0000000000
+
+
+def call(arlib, n=2, m=4, H=1024, eps=1e-6, mode=0, parts=None, res=None, w=None, out=None,
+         rout=None, sum_out=None):
+    span = m * H * 2 + 4096
+    parts = parts if parts is not None else [BASE + k * span for k in range(n)]
+    res = BASE + 20 * span if res is None else res
+    w = BASE + 21 * span if w is None else w
+    out = BASE + 22 * span if out is None else out
+    rout = BASE + 23 * span if rout is None else rout
+    arr = (ctypes.c_void_p * max(len(parts), 1))(*parts)
+    return arlib.lib().ar_rmsnorm_ex(arr, n, res, w, eps, m, H, out, rout, mode, None,
+                                     sum_out, None)
+
+
+def test_empty_call_is_a_noop(arlib):
+    assert call(arlib, m=0) == OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=0), ARG), (dict(n=17), ARG), (dict(m=-1), ARG), (dict(H=0), ARG),
+    (dict(eps=-1.0), ARG), (dict(eps=float("nan")), ARG), (dict(eps=float("inf")), ARG),
+    (dict(mode=3), ARG), (dict(H=1020), ALIGN), (dict(H=131072 + 8), UNSUPPORTED),
+])
+def test_bad_shapes(arlib, kw, status):
+    assert call(arlib, **kw) == status
+
+
+def test_null_and_misaligned_pointers(arlib):
+    assert call(arlib, res=0) == ARG
+    assert call(arlib, parts=[BASE, 0]) == ARG
+    assert call(arlib, out=BASE + 22 * (4 * 1024 * 2 + 4096) + 8) == ALIGN
+    assert call(arlib, parts=[BASE + 2, BASE + 100000]) == ALIGN
+    assert call(arlib, sum_out=BASE + 30 * 100000 + 4) == ALIGN
+
+
+def test_empty_call_needs_no_pointers(arlib):
+    assert call(arlib, m=0, res=0, out=0, rout=0, parts=[0, 0]) == OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="would launch on fake pointers")
+def test_in_place_residual_passes_the_checks(arlib):
+    # Without a device the call gets past every argument check and stops at
+    # the first CUDA call: AR_ERR_CUDA, not AR_ERR_ALIAS.
+    span = 4 * 1024 * 2 + 4096
+    res = BASE + 20 * span
+    assert call(arlib, res=res, rout=res) == CUDA
+
+
+def test_aliasing_rules(arlib):
+    span = 4 * 1024 * 2 + 4096
+    res = BASE + 20 * span
+    # everything that overlaps, other than residual_out == residual, is refused
+    assert call(arlib, out=res) == ALIAS
+    assert call(arlib, rout=res + 16) == ALIAS
+    assert call(arlib, out=BASE) == ALIAS                       # out over partial 0
+    assert call(arlib, rout=BASE + span + 64) == ALIAS          # residual_out inside partial 1
+    assert call(arlib, out=BASE + 30 * span, rout=BASE + 30 * span + 1024) == ALIAS
+    assert call(arlib, sum_out=res) == ALIAS
+
+
+def test_stage_entry_points_check_arguments(arlib):
+    L = arlib.lib()
+    arr = (ctypes.c_void_p * 2)(BASE, BASE + (1 << 20))
+    assert L.ar_reduce_scatter_flat(arr, 2, 12, BASE + (4 << 20), None) == ALIGN
+    assert L.ar_reduce_scatter_flat(arr, 0, 16, BASE + (4 << 20), None) == ARG
+    assert L.ar_reduce_scatter_flat(arr, 2, 16, BASE, None) == ALIAS
+    assert L.ar_reduce_scatter_flat(arr, 2, 0, BASE + (4 << 20), None) == OK
+    assert L.ar_load_rmsnorm(BASE, BASE + 4096, BASE + 8192, 1e-6, 0, 1024, BASE + 12288,
+                             BASE + 16384, None) == OK
+    assert L.ar_load_rmsnorm(BASE, BASE + 4096, BASE + 8192, -1.0, 1, 1024, BASE + 12288,
+                             BASE + 16384, None) == ARG
+
+
+def test_select_mode_is_host_logic(arlib):
+    for n in (1, 2, 4, 8, 16):
+        for m in (1, 16, 32, 1024, 16384):
+            assert arlib.ar_select_mode(n, m, 7168) in (1, 2)
+    with pytest.raises(arlib.ArError):
+        arlib.ar_select_mode(0, 1, 1024)
+
+
+SHAPES = [(2, 4, 1024), (8, 1, 7168), (8, 16, 7168), (4, 32, 7168), (4, 2048, 7168),
+          (8, 8192, 6144), (4, 1, 4096), (8, 16384, 8192), (1, 3, 8), (16, 5, 131072),
+          (3, 1000, 65536), (8, 151, 7168), (8, 152, 7168), (8, 304, 7168)]
+
+
+@pytest.mark.parametrize("n,m,H", SHAPES)
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_plan_covers_every_pack(arlib, n, m, H, mode):
+    p = arlib.ar_get_plan(n, m, H, mode, sm_count=152)
+    P = H // 8
+    per_cta = -(-P // p["cluster"])
+    assert p["mode"] in (1, 2) and (mode == 0 or p["mode"] == mode)
+    assert p["cluster"] in (1, 2, 4, 8, 16) and p["vpt"] in (1, 2, 4, 8)
+    assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024 // p["vpt"]
+    assert p["threads"] * p["vpt"] >= per_cta          # every pack has an owner
+    assert per_cta <= 1024                             # a CTA holds its row slice in registers
+    assert p["ctas"] == m * p["cluster"]
+    assert p["launches"] == (2 if p["mode"] == 2 else 1)
+
+
+def test_plan_spreads_small_batches(arlib):
+    # decode: a single row of H = 7168 spreads over a 16-CTA cluster
+    assert arlib.ar_get_plan(8, 1, 7168, 1, sm_count=152)["cluster"] == 16
+    # prefill: rows alone fill the GPU; one CTA per row
+    assert arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)["cluster"] == 1
+
+
+def test_plan_rejects_bad_shapes(arlib):
+    with pytest.raises(arlib.ArError):
+        arlib.ar_get_plan(8, 4, 1020, 1, sm_count=152)
+    with pytest.raises(arlib.ArError):
+        arlib.ar_get_plan(8, 4, 1024, 7, sm_count=152)

@@ -1,0 +1,313 @@
+"""CUDA path (through the C ABI) against the CPU oracle, element by element.
+
+The reduced sum and residual_out must be bit-exact, out within
+2^-7 |ref| + 1e-3.  Covers the five workloads at their full sizes (small ones
+compared in full, large ones on sampled rows), every rank count, every
+launch shape, ragged and degenerate shapes, in-place residual, graph
+capture, non-default streams, guard bands around outputs and the argument
+errors that need a device.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import allreduce_sum_residual_gb300 as arn
+import synth
+from gpu_helpers import (compare, device_inputs, is_two_stage, oracle_rows, run_gpu,
+                         sample_rows, to_f32)
+
+pytestmark = pytest.mark.gpu
+
+MAX_WS = 16384 * 8192
+
+
+@pytest.fixture(scope="module", autouse=True)
+def workspace(arlib):
+    torch.cuda.set_device(0)
+    arn.ar_reserve_workspace(MAX_WS, 0)
+    yield
+
+
+def check_full(inp, mode, tag, **kw):
+    n, (m, H) = len(inp.partials), inp.residual.shape
+    gpu = run_gpu(inp, mode, **kw)
+    torch.cuda.synchronize()
+    orc = oracle_rows(inp, None, is_two_stage(n, m, H, mode))
+    return compare(gpu, orc, tag)
+
+
+def check_sampled(inp, mode, tag, k=48):
+    n, (m, H) = len(inp.partials), inp.residual.shape
+    out, rout, s = run_gpu(inp, mode)
+    torch.cuda.synchronize()
+    rows = sample_rows(m, k)
+    idx = torch.as_tensor(rows, device=out.device)
+    orc = oracle_rows(inp, rows, is_two_stage(n, m, H, mode))
+    return compare((out[idx], rout[idx], s[idx]), orc, tag)
+
+
+# ------------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage", "auto"])
+def test_tiny(mode):
+    w = synth.TINY
+    check_full(device_inputs(w, w.ms[0]), mode, f"tiny/{mode}")
+
+
+@pytest.mark.parametrize("m", synth.DECODE.ms)
+@pytest.mark.parametrize("mode", ["one_stage", "auto"])
+def test_decode(m, mode):
+    check_full(device_inputs(synth.DECODE, m), mode, f"decode m={m}/{mode}")
+
+
+@pytest.mark.parametrize("m", synth.TWO_STAGE.ms)
+@pytest.mark.parametrize("mode", ["two_stage", "one_stage", "auto"])
+def test_two_stage_workload(m, mode):
+    check_full(device_inputs(synth.TWO_STAGE, m), mode, f"two_stage m={m}/{mode}")
+
+
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage", "auto"])
+def test_prefill_full(mode):
+    w = synth.PREFILL
+    check_full(device_inputs(w, w.ms[0]), mode, f"prefill/{mode}")
+
+
+@pytest.mark.parametrize("w", synth.SWEEP, ids=lambda w: w.name)
+def test_sweep_auto(w):
+    for m in w.ms:
+        inp = device_inputs(w, m, seed=m)
+        if m * w.H <= 1024 * 8192:
+            check_full(inp, "auto", f"{w.name} m={m}")
+        else:
+            check_sampled(inp, "auto", f"{w.name} m={m}")
+        del inp
+        torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ structure
+
+@pytest.mark.parametrize("n", range(1, 17))
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_every_rank_count(n, mode):
+    w = synth.Workload("ranks", n=n, H=1032, ms=(7,), p_std=0.5, res_std=1.0, seed=n)
+    check_full(device_inputs(w, 7), mode, f"n={n}/{mode}")
+
+
+def wide_range_inputs(n, m, H, seed):
+    """Magnitudes spread over 2^-16 .. 2^16 so that the order of the fp32 adds
+    changes the result in many elements."""
+    rng = np.random.default_rng(seed)
+    parts = []
+    for _ in range(n):
+        x = rng.standard_normal((m, H)).astype(np.float32) * np.exp2(
+            rng.integers(-16, 17, (m, H))).astype(np.float32)
+        parts.append(torch.from_numpy(x).to(torch.bfloat16).cuda())
+    res = torch.from_numpy(rng.standard_normal((m, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    wt = torch.from_numpy((1 + 0.1 * rng.standard_normal(H)).astype(np.float32)).to(torch.bfloat16).cuda()
+    return synth.Inputs(parts, res, wt, 1e-6)
+
+
+@pytest.mark.parametrize("n", [3, 8, 16])
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_order_sensitive_inputs(n, mode):
+    inp = wide_range_inputs(n, 33, 2048, seed=n)
+    # the data really is order sensitive: a reversed-order fp32 sum differs
+    f = [synth.bits(p).astype(np.uint32) << 16 for p in inp.partials]
+    fwd = f[0].view(np.float32).copy()
+    for x in f[1:]:
+        fwd = fwd + x.view(np.float32)
+    rev = f[-1].view(np.float32).copy()
+    for x in f[-2::-1]:
+        rev = rev + x.view(np.float32)
+    assert np.mean(fwd != rev) > 0.01
+    check_full(inp, mode, f"order-sensitive n={n}/{mode}")
+
+
+SHAPES = [(c, v) for c in (1, 2, 4, 8, 16) for v in (1, 2, 4, 8)]
+
+
+@pytest.mark.parametrize("cluster,vpt", SHAPES)
+def test_launch_shape_does_not_change_results(cluster, vpt):
+    inp = wide_range_inputs(8, 5, 7168, seed=1)
+    m, H = inp.residual.shape
+    if -(-(H // 8) // cluster) > 1024:
+        pytest.skip("a CTA holds at most 1024 packs")
+    ref = run_gpu(inp, "one_stage")
+    got = run_gpu(inp, "one_stage", cluster=cluster, vpt=vpt)
+    torch.cuda.synchronize()
+    assert torch.equal(ref[2].view(torch.int32), got[2].view(torch.int32))
+    assert torch.equal(ref[1].view(torch.int16), got[1].view(torch.int16))
+    check_full(inp, "one_stage", f"cluster={cluster} vpt={vpt}", cluster=cluster, vpt=vpt)
+
+
+@pytest.mark.parametrize("m,H", [(1, 8), (3, 24), (2, 1032), (5, 7176), (153, 4104), (1, 131072),
+                                 (2, 65544), (300, 8)])
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_ragged_and_extreme_shapes(m, H, mode):
+    w = synth.Workload("ragged", n=3, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=H)
+    check_full(device_inputs(w, m), mode, f"m={m} H={H}/{mode}")
+
+
+def guarded(m, H):
+    """An [m, H] bf16 view inside a buffer with 4 KiB guard bands each side,
+    every guard element holding the pattern 0x5A5A."""
+    g = 2048
+    buf = torch.full((m * H + 2 * g,), 0x5A5A, dtype=torch.int16, device="cuda")
+    return buf, buf[g:g + m * H].view(torch.bfloat16).view(m, H), g
+
+
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+@pytest.mark.parametrize("m,H", [(1, 8), (7, 1032), (19, 7168)])
+def test_outputs_stay_inside_their_buffers(mode, m, H):
+    w = synth.Workload("guard", n=4, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m)
+    bo, out, g = guarded(m, H)
+    br, rout, _ = guarded(m, H)
+    bs = torch.full((m * H + 2 * 1024,), 7.0, dtype=torch.float32, device="cuda")
+    s = bs[1024:1024 + m * H].view(m, H)
+    arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, inp.eps, out=out, residual_out=rout,
+                      mode=mode, sum_out=s)
+    torch.cuda.synchronize()
+    for b in (bo, br):
+        assert torch.all(b[:g] == 0x5A5A) and torch.all(b[g + m * H:] == 0x5A5A)
+    assert torch.all(bs[:1024] == 7.0) and torch.all(bs[1024 + m * H:] == 7.0)
+    orc = oracle_rows(inp, None, mode == "two_stage")
+    compare((out, rout, s), orc, f"guarded {mode}")
+
+
+def test_empty_batch_launches_nothing():
+    w = synth.DECODE
+    inp = device_inputs(w, 1)
+    z = [torch.empty((0, w.H), dtype=torch.bfloat16, device="cuda") for _ in range(w.n)]
+    res = torch.empty((0, w.H), dtype=torch.bfloat16, device="cuda")
+    out, rout = arn.ar_rmsnorm(z, res, inp.weight, w.eps)
+    assert out.shape == (0, w.H) and rout.shape == (0, w.H)
+
+
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_in_place_residual(mode):
+    w = synth.DECODE
+    inp = device_inputs(w, 16)
+    orc = oracle_rows(inp, None, mode == "two_stage")
+    res_copy = inp.residual.clone()
+    out, rout = arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps,
+                               residual_out=inp.residual, mode=mode)
+    torch.cuda.synchronize()
+    assert rout.data_ptr() == inp.residual.data_ptr()
+    assert not torch.equal(res_copy, inp.residual)
+    compare((out, rout, None), orc, f"in-place {mode}")
+
+
+def test_n1_two_stage_equals_one_stage():
+    w = synth.Workload("n1", n=1, H=4096, ms=(64,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, 64)
+    a = run_gpu(inp, "one_stage")
+    b = run_gpu(inp, "two_stage")
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.view(torch.int16) if x.dtype == torch.bfloat16 else x.view(torch.int32),
+                           y.view(torch.int16) if y.dtype == torch.bfloat16 else y.view(torch.int32))
+
+
+@pytest.mark.parametrize("scale", [1e15, 1e-15])
+def test_large_and_small_magnitudes_and_zero_rows(scale):
+    """Magnitudes far from 1 (the fp32 square sum stays finite while
+    H * max r^2 < 3.4e38, so 1e15 is in range) and an all-zero row."""
+    w = synth.Workload("big", n=4, H=1024, ms=(4,), p_std=scale, res_std=scale)
+    inp = device_inputs(w, 4)
+    for p in inp.partials:
+        p[2].zero_()
+    inp.residual[2].zero_()
+    check_full(inp, "one_stage", "large magnitudes")
+    check_full(inp, "two_stage", "large magnitudes two-stage")
+
+
+# ------------------------------------------------------------------ stages
+
+def test_stage_entry_points():
+    w = synth.TWO_STAGE
+    inp = device_inputs(w, 64)
+    m, H = inp.residual.shape
+    temp = torch.empty((m, H), dtype=torch.bfloat16, device="cuda")
+    arn.ar_reduce_scatter_flat(inp.partials, temp)
+    out, rout = arn.ar_load_rmsnorm(temp, inp.residual, inp.weight, w.eps)
+    torch.cuda.synchronize()
+    o_out, o_rout, o_sum = oracle_rows(inp, None, two_stage=True)
+    assert np.array_equal(to_f32(synth.bits(temp)), o_sum)       # stage 1 bit-exact
+    compare((out, rout, None), (o_out, o_rout, o_sum), "stage 2")
+
+
+# ------------------------------------------------------------------ runtime
+
+def test_graph_capture_and_replay():
+    w = synth.DECODE
+    inp = device_inputs(w, 8)
+    s = torch.cuda.Stream()
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    with torch.cuda.stream(s):
+        arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, out=out, residual_out=rout,
+                       mode="two_stage")
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for mode in ("one_stage", "two_stage"):
+            arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, out=out,
+                           residual_out=rout, mode=mode)
+    out.zero_()
+    rout.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    compare((out, rout, None), oracle_rows(inp, None, True), "graph replay")
+
+
+def test_non_default_stream():
+    w = synth.DECODE
+    inp = device_inputs(w, 4)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out, rout, sm = run_gpu(inp, "one_stage")
+    s.synchronize()
+    compare((out, rout, sm), oracle_rows(inp, None, False), "side stream")
+
+
+def test_workspace_errors():
+    w = synth.TWO_STAGE
+    inp = device_inputs(w, 32)
+    arn.ar_release_workspace(0)
+    assert arn.ar_workspace_elems(0) == 0
+    with pytest.raises(arn.ArError) as e:
+        arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, mode="two_stage")
+    assert e.value.status == arn.AR_ERR_WORKSPACE
+    arn.ar_reserve_workspace(16 * w.H, 0)
+    with pytest.raises(arn.ArError) as e:
+        arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, mode="two_stage")
+    assert e.value.status == arn.AR_ERR_WORKSPACE
+    arn.ar_reserve_workspace(MAX_WS, 0)
+    assert arn.ar_workspace_elems(0) >= MAX_WS
+    check_full(inp, "two_stage", "after re-reserve")
+
+
+def test_plan_matches_device():
+    p = arn.ar_get_plan(8, 1, 7168, 0)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert p == arn.ar_get_plan(8, 1, 7168, 0, sm_count=sms)
+
+
+def test_raw_c_abi_call():
+    """The plain C entry point with raw pointers (no binding helpers)."""
+    w = synth.TINY
+    inp = device_inputs(w, 4)
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    L = arn.lib()
+    arr = (ctypes.c_void_p * w.n)(*[p.data_ptr() for p in inp.partials])
+    st = L.ar_rmsnorm(arr, w.n, inp.residual.data_ptr(), inp.weight.data_ptr(), w.eps, 4, w.H,
+                      out.data_ptr(), rout.data_ptr(), 1,
+                      torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    torch.cuda.synchronize()
+    compare((out, rout, None), oracle_rows(inp, None, False), "raw C ABI")
