@@ -15,7 +15,8 @@ Names follow the C ABI:
     ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None)
     ar_reserve_workspace(max_elems, device) / ar_release_workspace(device)
     ar_workspace_elems(device), ar_select_mode(n, m, H),
-    ar_get_plan(n, m, H, mode, sm_count=0), ar_strerror(status), ar_version()
+    ar_get_plan(n, m, H, mode, sm_count=0), ar_device_status(device, reset),
+    ar_selftest_bounded_wait(device, limit_us), ar_strerror(status), ar_version()
 """
 import ctypes
 import os
@@ -46,9 +47,16 @@ class ArError(RuntimeError):
         super().__init__(f"{what}: status {status} ({_strerror(status)})")
 
 
+AR_KERNEL_AUTO = 0
+AR_KERNEL_REGISTER = 1
+AR_KERNEL_STREAM = 2
+KERNELS = {"auto": AR_KERNEL_AUTO, "register": AR_KERNEL_REGISTER, "stream": AR_KERNEL_STREAM}
+
+
 class ar_plan_t(ctypes.Structure):
-    _fields_ = [("mode", ctypes.c_int), ("cluster", ctypes.c_int), ("vpt", ctypes.c_int),
-                ("threads", ctypes.c_int), ("ctas", ctypes.c_int64), ("launches", ctypes.c_int)]
+    _fields_ = [("mode", ctypes.c_int), ("kernel", ctypes.c_int), ("cluster", ctypes.c_int),
+                ("vpt", ctypes.c_int), ("threads", ctypes.c_int), ("stages", ctypes.c_int),
+                ("ctas", ctypes.c_int64), ("launches", ctypes.c_int)]
 
 
 _lib = None
@@ -69,6 +77,8 @@ _SIGS = {
     "ar_release_workspace": (ctypes.c_int, [ctypes.c_int]),
     "ar_workspace_elems": (_I64, [ctypes.c_int]),
     "ar_select_mode": (ctypes.c_int, [ctypes.c_int, _I64, _I64]),
+    "ar_device_status": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
+    "ar_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint]),
     "ar_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ar_version": (ctypes.c_int, []),
 }
@@ -167,10 +177,11 @@ def ar_rmsnorm(partials, residual, weight, eps, out=None, residual_out=None,
 
 
 def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
-                  mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0):
+                  mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0, kernel=0):
     """ar_rmsnorm plus the reduced sum (fp32 [m, H] ``sum_out``) and a forced
-    launch shape (``cluster`` CTAs per row, ``vpt`` packs per thread; 0 =
-    library's choice).  Returns (out, residual_out, sum_out)."""
+    kernel ("register" / "stream") and register-kernel launch shape
+    (``cluster`` CTAs per row, ``vpt`` packs per thread); 0 = library's
+    choice.  Returns (out, residual_out, sum_out)."""
     import torch
     mode = MODES.get(mode, mode)
     m, H, dev, out, residual_out, arr = _prepare(partials, residual, weight, out, residual_out)
@@ -179,8 +190,9 @@ def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
                 not sum_out.is_contiguous() or sum_out.device != dev:
             raise ValueError("sum_out must be a contiguous float32 [m, H] tensor on the inputs' device")
     plan = None
-    if cluster or vpt:
-        plan = ctypes.pointer(ar_plan_t(0, int(cluster), int(vpt), 0, 0, 0))
+    kernel = KERNELS.get(kernel, kernel)
+    if cluster or vpt or kernel:
+        plan = ctypes.pointer(ar_plan_t(0, int(kernel), int(cluster), int(vpt), 0, 0, 0, 0))
     st = lib().ar_rmsnorm_ex(arr, len(partials), _ptr(residual), _ptr(weight), float(eps), m, H,
                              _ptr(out), _ptr(residual_out), int(mode), _stream_ptr(stream, dev),
                              _VP(sum_out.data_ptr()) if sum_out is not None else None, plan)
@@ -235,6 +247,17 @@ def ar_get_plan(n, m, H, mode=AR_MODE_AUTO, sm_count=0):
     _check(lib().ar_get_plan(int(n), int(m), int(H), int(MODES.get(mode, mode)), int(sm_count),
                              ctypes.byref(p)), "ar_get_plan")
     return {f: getattr(p, f) for f, _ in ar_plan_t._fields_}
+
+
+def ar_device_status(device=0, reset=False):
+    """AR_OK, or AR_ERR_TIMEOUT after a bounded in-kernel wait gave up
+    (synchronises the device)."""
+    return int(lib().ar_device_status(int(device), int(bool(reset))))
+
+
+def ar_selftest_bounded_wait(device=0, limit_us=1000):
+    """Run the bounded-wait self-test kernel; returns the status it left."""
+    return int(lib().ar_selftest_bounded_wait(int(device), int(limit_us)))
 
 
 def ar_strerror(status):

@@ -6,6 +6,12 @@
 #include <mutex>
 
 #include "epilogue.cuh"
+#include "stream_epilogue.cuh"
+
+// The device status word: AR_OK, or AR_ERR_TIMEOUT after a bounded wait in a
+// kernel gave up.  One per device (every device that loads the module holds
+// its own copy); kernels receive its address.
+__device__ int g_arn_status;
 
 namespace arn {
 
@@ -14,6 +20,14 @@ EpilogueKernel epilogue_kernel_group1(int n, int vpt_log2);
 EpilogueKernel epilogue_kernel_group2(int n, int vpt_log2);
 EpilogueKernel epilogue_kernel_group3(int n, int vpt_log2);
 cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream);
+StreamKernel stream_kernel_group0(int n, int vpt_log2);
+StreamKernel stream_kernel_group1(int n, int vpt_log2);
+StreamKernel stream_kernel_group2(int n, int vpt_log2);
+StreamKernel stream_kernel_group3(int n, int vpt_log2);
+cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t s);
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
+constexpr int kAssumedSmemOptin = 232448;         // sm_100-class opt-in per CTA (host-only plans)
 
 static int vpt_log2(int vpt) { return vpt == 1 ? 0 : vpt == 2 ? 1 : vpt == 4 ? 2 : vpt == 8 ? 3 : -1; }
 
@@ -28,6 +42,17 @@ EpilogueKernel epilogue_kernel(int n, int vpt) {
   }
 }
 
+StreamKernel stream_kernel(int n, int vpt) {
+  const int l = vpt_log2(vpt);
+  if (n < 1 || n > AR_MAX_RANKS || l < 0) return nullptr;
+  switch ((n - 1) / 4) {
+    case 0: return stream_kernel_group0(n, l);
+    case 1: return stream_kernel_group1(n, l);
+    case 2: return stream_kernel_group2(n, l);
+    default: return stream_kernel_group3(n, l);
+  }
+}
+
 // ---------------------------------------------------------------- per-device state
 
 constexpr int kMaxDevices = 64;
@@ -35,6 +60,8 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
   bool ready = false;        // attributes read and kernel attributes set
   int sms = 0;
+  int smem_optin = 0;        // largest dynamic shared memory per CTA
+  int *status = nullptr;     // this device's g_arn_status
   void *workspace = nullptr; // two-stage bf16 temporary
   int64_t workspace_elems = 0;
 };
@@ -54,11 +81,24 @@ static DeviceState *current_device(int *status) {
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState &d = g_dev[dev];
   if (!d.ready) {
-    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess ||
+        cudaGetSymbolAddress(reinterpret_cast<void **>(&d.status), g_arn_status) != cudaSuccess) {
       cudaGetLastError();
       *status = AR_ERR_CUDA;
       return nullptr;
     }
+    for (int n = 1; n <= AR_MAX_RANKS; ++n)
+      for (int vpt = 1; vpt <= 8; vpt *= 2) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(stream_kernel(n, vpt)),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, d.smem_optin) !=
+            cudaSuccess) {
+          cudaGetLastError();
+          *status = AR_ERR_CUDA;
+          return nullptr;
+        }
+      }
     // Rows split over up to 16 CTAs need the non-portable cluster size.
     for (int n = 1; n <= AR_MAX_RANKS; ++n)
       for (int vpt = 1; vpt <= 8; vpt *= 2) {
@@ -144,7 +184,11 @@ static int select_mode(int n, int64_t m, int64_t H) {
   return m <= one_stage_max_rows(n, H) ? AR_MODE_ONE_STAGE : AR_MODE_TWO_STAGE;
 }
 
-// Launch shape of the epilogue kernel for m rows of P packs with n inputs.
+// The stream kernel takes over from this many rows on (rows alone then give
+// every SM several rows to stream through its ring).
+static int64_t stream_min_rows(int sms) { return 2 * static_cast<int64_t>(sms); }
+
+// Register kernel: launch shape for m rows of P packs.
 //  * cluster S: the fewest CTAs per row that hold a row in registers
 //    (<= 1024 packs per CTA), then doubled while the grid (m * S) does not
 //    yet give every SM a CTA and each CTA keeps >= 32 packs.
@@ -152,7 +196,7 @@ static int select_mode(int n, int64_t m, int64_t H) {
 //    thread that keep a CTA at <= 256 threads (several CTAs per SM);
 //    otherwise 1 pack per thread, i.e. the most loads in flight at once
 //    for a short grid.  Either way a CTA stays within 1024 / vpt threads.
-static void plan_epilogue(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
+static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
                           ar_plan_t *pl) {
   int S = 1;
   while (S < kMaxClusterCtas && (P + S - 1) / S > kMaxPacksPerCta) S *= 2;
@@ -166,29 +210,69 @@ static void plan_epilogue(int64_t m, int64_t P, int sms, int force_cluster, int 
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
   threads = (threads + 31) / 32 * 32;
+  pl->kernel = AR_KERNEL_REGISTER;
   pl->cluster = S;
   pl->vpt = vpt;
   pl->threads = threads;
+  pl->stages = 0;
   pl->ctas = m * S;
 }
 
-static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, const ar_plan_t *force,
-                     ar_plan_t *pl) {
+static int64_t stream_smem_bytes(int inputs, int consumers, int stages) {
+  return static_cast<int64_t>(stages) * (inputs + 1) * consumers * 16 + 16 * stages + 64 * 4 + 16;
+}
+
+// Stream kernel: a row is split into V tiles of T_c <= 512 packs (about 256
+// where that gives <= 8 tiles); the ring holds as many slots of (inputs + 1)
+// tiles as fit in shared memory, at most 16.  False if it cannot apply.
+static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_optin, ar_plan_t *pl) {
+  if (P > AR_STREAM_MAX_HIDDEN / kPackElems) return false;
+  int64_t V = (P + 255) / 256;
+  if (V > 8) V = (P + kStreamMaxConsumers - 1) / kStreamMaxConsumers;
+  if (V > 8) return false;
+  const int Tc = static_cast<int>(((P + V - 1) / V + 31) / 32 * 32);
+  int stages = 16;
+  while (stages >= 2 && stream_smem_bytes(inputs, Tc, stages) > smem_optin) --stages;
+  if (stages < 2) return false;
+  int vpt = 1;
+  while (vpt < V) vpt *= 2;
+  pl->kernel = AR_KERNEL_STREAM;
+  pl->cluster = 1;
+  pl->vpt = vpt;
+  pl->threads = 32 + Tc;
+  pl->stages = stages;
+  pl->ctas = m < sms ? m : sms;
+  return true;
+}
+
+static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
+                     const ar_plan_t *force, ar_plan_t *pl) {
   if (mode != AR_MODE_AUTO && mode != AR_MODE_ONE_STAGE && mode != AR_MODE_TWO_STAGE)
     return AR_ERR_ARG;
   std::memset(pl, 0, sizeof *pl);
   pl->mode = mode == AR_MODE_AUTO ? select_mode(n, m, H) : mode;
-  int fc = 0, fv = 0;
+  int fk = AR_KERNEL_AUTO, fc = 0, fv = 0;
   if (force) {
+    fk = force->kernel;
     fc = force->cluster;
     fv = force->vpt;
+    if (fk != AR_KERNEL_AUTO && fk != AR_KERNEL_REGISTER && fk != AR_KERNEL_STREAM)
+      return AR_ERR_ARG;
     if (fc != 0 && fc != 1 && fc != 2 && fc != 4 && fc != 8 && fc != 16) return AR_ERR_ARG;
     if (fv != 0 && vpt_log2(fv) < 0) return AR_ERR_ARG;
+    if (fk == AR_KERNEL_STREAM && (fc > 1 || fv != 0)) return AR_ERR_ARG;
   }
   const int64_t P = H / kPackElems;
-  plan_epilogue(m, P, sms, fc, fv, pl);
-  const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;
-  if (per_cta > static_cast<int64_t>(pl->vpt) * (1024 / pl->vpt)) return AR_ERR_ARG;  // forced shape too small
+  const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
+  const bool shape_forced = fc != 0 || fv != 0;
+  const bool want_stream =
+      fk == AR_KERNEL_STREAM || (fk == AR_KERNEL_AUTO && !shape_forced && m >= stream_min_rows(sms));
+  if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin, pl))) {
+    if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
+    plan_register(m, P, sms, fc, fv, pl);
+    const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;
+    if (per_cta > kMaxPacksPerCta) return AR_ERR_ARG;  // forced shape too small
+  }
   if (pl->ctas > INT32_MAX) return AR_ERR_UNSUPPORTED;
   pl->launches = pl->mode == AR_MODE_TWO_STAGE ? 2 : 1;
   return AR_OK;
@@ -212,6 +296,32 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
   }
   const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt), a);
   if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_stream(const void *const *inputs, int n, const void *residual,
+                                 const void *weight, float eps, int64_t m, int64_t H, void *out,
+                                 void *residual_out, float *sum_out, const ar_plan_t &pl,
+                                 int *status, cudaStream_t stream) {
+  StreamArgs a;
+  std::memset(&a, 0, sizeof a);
+  for (int k = 0; k < n; ++k) a.src[k] = static_cast<const uint4 *>(inputs[k]);
+  a.src[n] = static_cast<const uint4 *>(residual);
+  a.w = static_cast<const uint4 *>(weight);
+  a.out = static_cast<uint4 *>(out);
+  a.rout = static_cast<uint4 *>(residual_out);
+  a.sum = reinterpret_cast<float4 *>(sum_out);
+  a.m = m;
+  a.P = static_cast<int>(H / kPackElems);
+  const int Tc = pl.threads - 32;
+  a.tiles = (a.P + Tc - 1) / Tc;
+  a.stages = pl.stages;
+  a.H = static_cast<float>(H);
+  a.eps = eps;
+  a.wait_limit_ns = kWaitLimitNs;
+  a.status = status;
+  const size_t smem = static_cast<size_t>(stream_smem_bytes(n, Tc, pl.stages));
+  stream_kernel(n, pl.vpt)<<<static_cast<unsigned>(pl.ctas), pl.threads, smem, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -246,14 +356,24 @@ static int run(const void *const *partials, int n, const void *residual, const v
   DeviceState *d = current_device(&st);
   if (!d) return st;
   ar_plan_t pl;
-  st = make_plan(n, m, H, mode, d->sms, force, &pl);
+  st = make_plan(n, m, H, mode, d->sms, d->smem_optin, force, &pl);
   if (st != AR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  EpilogueArgs a;
-  if (pl.mode == AR_MODE_ONE_STAGE) {
-    fill_epilogue_args(&a, partials, n, residual, weight, eps, m, H, out, residual_out, sum_out, pl);
-    return launch_epilogue(a, n, pl, s) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
-  }
+  // The epilogue over `inputs` (the partials, or the two-stage temporary).
+  auto epilogue = [&](const void *const *inputs, int count) -> int {
+    cudaError_t e;
+    if (pl.kernel == AR_KERNEL_STREAM) {
+      e = launch_stream(inputs, count, residual, weight, eps, m, H, out, residual_out, sum_out, pl,
+                        d->status, s);
+    } else {
+      EpilogueArgs a;
+      fill_epilogue_args(&a, inputs, count, residual, weight, eps, m, H, out, residual_out,
+                         sum_out, pl);
+      e = launch_epilogue(a, count, pl, s);
+    }
+    return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+  };
+  if (pl.mode == AR_MODE_ONE_STAGE) return epilogue(partials, n);
   // two-stage: stage 1 into the workspace, stage 2 from it
   void *ws;
   {
@@ -276,8 +396,7 @@ static int run(const void *const *partials, int n, const void *residual, const v
   ra.npacks = m * H / kPackElems;
   if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   const void *temp_in[1] = {ws};
-  fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, sum_out, pl);
-  return launch_epilogue(a, 1, pl, s) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+  return epilogue(temp_in, 1);
 }
 
 }  // namespace arn
@@ -304,12 +423,60 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count, ar_plan_t *
   if (!plan) return AR_ERR_ARG;
   int st = check_shape(n, m, H, 0.f);
   if (st != AR_OK) return st;
+  int smem = kAssumedSmemOptin;
   if (sm_count <= 0) {
     DeviceState *d = current_device(&st);
     if (!d) return st;
     sm_count = d->sms;
+    smem = d->smem_optin;
   }
-  return make_plan(n, m, H, mode, sm_count, nullptr, plan);
+  return make_plan(n, m, H, mode, sm_count, smem, nullptr, plan);
+}
+
+int ar_device_status(int device, int reset) {
+  if (device < 0 || device >= kMaxDevices) return AR_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  int st = AR_OK, value = AR_OK;
+  DeviceState *d = current_device(&st);
+  if (d) {
+    if (cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(&value, d->status, sizeof value, cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      st = AR_ERR_CUDA;
+    } else if (reset) {
+      const int zero = AR_OK;
+      if (cudaMemcpy(d->status, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        st = AR_ERR_CUDA;
+      }
+    }
+  }
+  cudaSetDevice(prev);
+  return st != AR_OK ? st : value;
+}
+
+int ar_selftest_bounded_wait(int device, unsigned limit_us) {
+  if (device < 0 || device >= kMaxDevices || limit_us == 0 || limit_us > 10000000u)
+    return AR_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  int st = AR_OK;
+  DeviceState *d = current_device(&st);
+  if (d) {
+    if (launch_bounded_wait_selftest(static_cast<uint64_t>(limit_us) * 1000u, d->status, nullptr) !=
+        cudaSuccess)
+      st = AR_ERR_CUDA;
+  }
+  cudaSetDevice(prev);
+  if (st != AR_OK) return st;
+  return ar_device_status(device, 1);
 }
 
 int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count, void *temp,

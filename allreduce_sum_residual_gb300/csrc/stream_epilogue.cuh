@@ -1,0 +1,279 @@
+// The fused epilogue for many rows: a persistent, warp-specialised kernel
+// that streams rows through shared memory with bulk asynchronous copies.
+//
+// Same arithmetic as k_fused_epilogue (rank-order fp32 sum of n partials,
+// residual add, RMSNorm; ROCm/aiter #3817 "perf: optimize fused AllReduce +
+// RMSNorm (custom_all_reduce)", Technical Details, 1stage), same ownership of
+// every element by one thread, so the sum and residual_out are bit-identical
+// to it.  What changes is how bytes reach the SM:
+//
+//   * one producer warp (lane 0) issues cp.async.bulk copies (the 1-D TMA
+//     path) of a row tile of every input -- the n partials and the residual,
+//     T_c packs each -- into a ring of S shared-memory slots, completing on
+//     the slot's "full" mbarrier with a transaction-byte count;
+//   * C consumer warps (T_c = 32*C threads) wait on "full", read their pack
+//     of each input from shared memory, keep r = sum + residual in
+//     registers, and release the slot on its "empty" mbarrier;
+//   * after the last tile of a row the consumers reduce the square sum among
+//     themselves (named barrier 1), then store residual_out and out.
+//
+// The CTA is persistent: CTA b handles rows b, b + G, b + 2G, ...  The
+// producer runs up to S tiles ahead, across row boundaries, so the next
+// row's loads overlap this row's reduction and stores, and the bytes in
+// flight per SM are bounded by shared memory rather than by registers.
+//
+// Every mbarrier wait is bounded (wait_limit_ns of %globaltimer): on timeout
+// the waiting thread records AR_ERR_TIMEOUT in a device status word, raises
+// the CTA's abort flag and stops; the producer stops issuing and drains the
+// copies it has in flight (again bounded) before the CTA exits.
+#pragma once
+
+#include "common.cuh"
+
+namespace arn {
+
+struct StreamArgs {
+  const uint4 *src[AR_MAX_RANKS + 1];  // partials in rank order, then the residual
+  const uint4 *w;                      // weight [H/8]
+  uint4 *out;                          // [m, H/8]
+  uint4 *rout;                         // [m, H/8]
+  float4 *sum;                         // optional fp32 sum, or null
+  int64_t m;
+  int P;                               // packs per row
+  int tiles;                           // tiles per row: ceil(P / T_c)
+  int stages;                          // ring slots
+  float H;
+  float eps;
+  uint64_t wait_limit_ns;              // bound of every mbarrier wait
+  int *status;                         // device status word (AR_ERR_TIMEOUT on timeout)
+};
+
+// --- mbarrier / bulk copy (PTX) ------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until phase `parity` of `bar` completes, for at most limit_ns.  On
+// timeout: record AR_ERR_TIMEOUT, raise the CTA's abort flag, return false.
+// Also returns false (without waiting) once another thread raised abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag, uint64_t limit_ns,
+                                                  int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      if (status) atomicExch(status, AR_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` on `bar`.  Addresses and
+// size are multiples of 16 bytes.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// --- the kernel -------------------------------------------------------------------
+
+// Dynamic shared memory: [stages][N + 1][T_c] uint4 slots, then 2*stages
+// mbarriers, then the reduction scratch and the abort flag.
+constexpr int kStreamMaxConsumers = 512;
+
+template <int N, int VPT>
+__global__ void __launch_bounds__(32 + kStreamMaxConsumers, 1)
+k_stream_epilogue(const __grid_constant__ StreamArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int Tc = static_cast<int>(blockDim.x) - 32;
+  const int S = a.stages;
+  uint4 *slots = reinterpret_cast<uint4 *>(smem);
+  const size_t slot_packs = static_cast<size_t>(N + 1) * Tc;
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + static_cast<size_t>(S) * slot_packs * 16);
+  uint64_t *empty = full + S;
+  float *red = reinterpret_cast<float *>(empty + S);  // [2][32]
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(red + 64);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int C = Tc >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], C);
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int64_t G = gridDim.x;
+  const int V = a.tiles;
+
+  if (warp == 0) {
+    // ---------------- producer
+    if (lane != 0) return;
+    int64_t t = 0;
+    for (int64_t row = blockIdx.x; row < a.m; row += G) {
+      for (int v = 0; v < V; ++v, ++t) {
+        const int s = static_cast<int>(t % S);
+        const int64_t k = t / S;
+        if (k > 0 && !mbar_wait_bounded(&empty[s], static_cast<uint32_t>((k - 1) & 1), abort_flag,
+                                        a.wait_limit_ns, a.status))
+          goto drain;
+        if (*abort_flag) goto drain;
+        const int c0 = v * Tc;
+        const int packs = min(Tc, a.P - c0);
+        const uint32_t bytes = static_cast<uint32_t>(packs) * 16u;
+        mbar_arrive_expect_tx(&full[s], bytes * (N + 1));
+        uint4 *dst = slots + static_cast<size_t>(s) * slot_packs;
+        const int64_t off = row * a.P + c0;
+#pragma unroll
+        for (int j = 0; j <= N; ++j) bulk_g2s(dst + static_cast<size_t>(j) * Tc, a.src[j] + off, bytes, &full[s]);
+      }
+    }
+  drain:
+    // Every slot's last issued fill must land before the CTA may exit.
+    for (int s = 0; s < S; ++s) {
+      if (t > s) {
+        const int64_t last = ((t - 1 - s) / S) * S + s;  // last tile issued into slot s
+        mbar_wait_bounded(&full[s], static_cast<uint32_t>((last / S) & 1), abort_flag,
+                          a.wait_limit_ns, a.status);
+      }
+    }
+    return;
+  }
+
+  // ---------------- consumers
+  const int tc = static_cast<int>(threadIdx.x) - 32;
+  const int cw = warp - 1;
+  // The weight is the same for every row: up to 4 tiles it stays in
+  // registers for the CTA's lifetime; wider rows re-read it (L1 hits).
+  constexpr int kWRegs = VPT <= 4 ? VPT : 1;
+  uint4 wv[kWRegs];
+#pragma unroll
+  for (int v = 0; v < kWRegs; ++v) {
+    const int c = v * Tc + tc;
+    wv[v] = (VPT <= 4 && v < V && c < a.P) ? ld_ro(a.w + c) : make_uint4(0, 0, 0, 0);
+  }
+
+  int64_t t = 0;
+  int parity_row = 0;
+  for (int64_t row = blockIdx.x; row < a.m; row += G, parity_row ^= 1) {
+    const int64_t base = row * a.P;
+    float r[VPT][8];
+    float ss = 0.f;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) r[v][e] = 0.f;
+      if (v < V) {
+        const int s = static_cast<int>(t % S);
+        // After an abort the consumers keep walking the rows without waiting
+        // or touching memory, so that every one of them still reaches each
+        // named barrier below.
+        const bool ok = mbar_wait_bounded(&full[s], static_cast<uint32_t>((t / S) & 1), abort_flag,
+                                          a.wait_limit_ns, a.status);
+        const int c = v * Tc + tc;
+        if (ok && c < a.P) {
+          const uint4 *slot = slots + static_cast<size_t>(s) * slot_packs + tc;
+          float acc[8], rs[8];
+          unpack8(slot[0], acc);
+#pragma unroll
+          for (int j = 1; j < N; ++j) {
+            float x[8];
+            unpack8(slot[static_cast<size_t>(j) * Tc], x);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = __fadd_rn(acc[e], x[e]);
+          }
+          unpack8(slot[static_cast<size_t>(N) * Tc], rs);
+          if (a.sum != nullptr) {
+            a.sum[2 * (base + c)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            a.sum[2 * (base + c) + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+          }
+#pragma unroll
+          for (int e = 0; e < 8; ++e) r[v][e] = __fadd_rn(acc[e], rs[e]);
+        }
+        __syncwarp();
+        if (lane == 0 && ok) mbar_arrive(&empty[s]);
+        ++t;
+      }
+    }
+    const bool live = !*abort_flag;
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = v * Tc + tc;
+      if (live && v < V && c < a.P) st_stream(a.rout + base + c, pack8(r[v]));
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss = fmaf(r[v][e], r[v][e], ss);
+    }
+    ss = warp_sum(ss);
+    float *rb = red + 32 * parity_row;
+    if (lane == 0) rb[cw] = ss;
+    named_barrier_sync(1, static_cast<uint32_t>(Tc));
+    float total = 0.f;
+    for (int i = 0; i < C; ++i) total += rb[i];
+    const float inv = rsqrtf(total / a.H + a.eps);
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = v * Tc + tc;
+      if (live && v < V && c < a.P) {
+        float w[8], y[8];
+        unpack8(VPT <= 4 ? wv[v < kWRegs ? v : 0] : ld_ro(a.w + c), w);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) y[e] = (r[v][e] * inv) * w[e];
+        st_stream(a.out + base + c, pack8(y));
+      }
+    }
+  }
+}
+
+using StreamKernel = void (*)(StreamArgs);
+StreamKernel stream_kernel(int n, int vpt);
+
+}  // namespace arn

@@ -360,14 +360,20 @@ def run_ours(args):
     rout = torch.empty_like(inp.residual)
     stream = torch.cuda.Stream(device)
     plan = arn.ar_get_plan(n, m, H, step_mode)
+    if args.kernel != "auto":
+        plan["kernel"] = arn.KERNELS[args.kernel]
     path = "two_stage" if plan["mode"] == 2 else "one_stage"
     props = torch.cuda.get_device_properties(device)
     l2 = getattr(props, "L2_cache_size", L2_BYTES_FALLBACK) or L2_BYTES_FALLBACK
 
     def step():
         with torch.cuda.stream(stream):
-            arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, inp.eps, out=out,
-                           residual_out=rout, mode=step_mode)
+            if args.kernel == "auto":
+                arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, inp.eps, out=out,
+                               residual_out=rout, mode=step_mode)
+            else:
+                arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, inp.eps, out=out,
+                                  residual_out=rout, mode=step_mode, kernel=args.kernel)
 
     with ClockSampler(local) as clk:
         total, per = timed_steps(step, stream, args.steps, args.warmup, world, device)
@@ -398,7 +404,8 @@ def run_ours(args):
                                                / statistics.mean(per_o) / 1e9, 1)}}
 
     peak, peak_kind = peaks()
-    kernel = "k_fused_epilogue" if path == "one_stage" else "k_reduce_flat"
+    kernel = ("k_reduce_flat" if path == "two_stage" else
+              "k_stream_epilogue" if plan["kernel"] == arn.AR_KERNEL_STREAM else "k_fused_epilogue")
     achieved = bytes_step / mean_step / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "kernel": kernel,
@@ -542,6 +549,8 @@ def main(argv=None):
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
     ap.add_argument("--mode", default="auto", choices=("auto", "one_stage", "two_stage"))
+    ap.add_argument("--kernel", default="auto", choices=("auto", "register", "stream"),
+                    help="force the epilogue kernel (profiling)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only the timed steps (no latency table, e2e or CPU baseline)")
     args = ap.parse_args(argv)

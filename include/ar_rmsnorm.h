@@ -84,6 +84,7 @@ extern "C" {
 
 #define AR_MAX_RANKS  16      /* most partials one call reduces                */
 #define AR_MAX_HIDDEN 131072  /* largest H (16 CTAs x 8192 columns)            */
+#define AR_STREAM_MAX_HIDDEN 32768 /* largest H of the stream kernel           */
 
 /*
  * The fused epilogue.
@@ -110,12 +111,23 @@ int ar_rmsnorm(const void *const *partials, int n, const void *residual,
  */
 typedef struct {
   int mode;        /* AR_MODE_ONE_STAGE or AR_MODE_TWO_STAGE                  */
-  int cluster;     /* CTAs sharing one row (a thread-block cluster), 1..16    */
-  int vpt;         /* 16-byte packs per thread: 1, 2, 4 or 8                  */
-  int threads;     /* threads per CTA                                          */
-  int64_t ctas;    /* CTAs of the epilogue kernel (m * cluster)               */
+  int kernel;      /* AR_KERNEL_REGISTER or AR_KERNEL_STREAM                   */
+  int cluster;     /* register kernel: CTAs sharing one row, 1..16            */
+  int vpt;         /* 16-byte packs per thread: 1, 2, 4 or 8 (stream kernel:
+                      row tiles per row, rounded up to a power of two)       */
+  int threads;     /* threads per CTA (stream kernel: 32 + consumers)         */
+  int stages;      /* stream kernel: shared-memory ring slots; else 0         */
+  int64_t ctas;    /* CTAs of the epilogue kernel                              */
   int launches;    /* kernels one call launches (1 or 2)                      */
 } ar_plan_t;
+
+/* Epilogue kernels (ar_plan_t.kernel). */
+#define AR_KERNEL_AUTO      0  /* library's choice (forcing only)             */
+#define AR_KERNEL_REGISTER  1  /* one CTA (or a cluster of up to 16) per row;
+                                  loads straight into registers: short grids */
+#define AR_KERNEL_STREAM    2  /* persistent, one CTA per SM; a producer warp
+                                  streams row tiles into a shared-memory ring
+                                  with bulk asynchronous copies: many rows   */
 
 /*
  * The plan ar_rmsnorm would follow for (n, m, H, mode) on a GPU with
@@ -132,12 +144,13 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count,
  *            reduced sum feeding the residual add: the fp32 accumulator for
  *            one-stage, the widened bf16 temporary for two-stage.  NULL to
  *            skip.  Costs 4*m*H extra bytes of writes.
- *   plan     NULL for the library's choice, else its `cluster` and `vpt`
- *            fields force the launch shape of the epilogue kernel (0 =
- *            library's choice; cluster in {1,2,4,8,16}, vpt in {1,2,4,8},
- *            and a CTA may cover at most 1024 packs, else AR_ERR_ARG).  The
- *            other fields are ignored; `mode` still picks the path.  The
- *            results do not depend on the launch shape.
+ *   plan     NULL for the library's choice, else its `kernel`, `cluster`
+ *            and `vpt` fields force the epilogue kernel and, for the register
+ *            kernel, its launch shape (0 = library's choice; cluster in
+ *            {1,2,4,8,16}, vpt in {1,2,4,8}, at most 1024 packs per CTA; the
+ *            stream kernel needs H <= 32768; else AR_ERR_ARG).  The other
+ *            fields are ignored; `mode` still picks the path.  The results
+ *            do not depend on the kernel or the launch shape.
  */
 int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
                   const void *weight, float eps, int64_t m, int64_t H,
@@ -186,6 +199,22 @@ int64_t ar_workspace_elems(int device);
  * Returns -AR_ERR_ARG for n outside [1, AR_MAX_RANKS], m < 0 or H <= 0.
  */
 int ar_select_mode(int n, int64_t m, int64_t H);
+
+/*
+ * The device status word of `device`: AR_OK, or AR_ERR_TIMEOUT once a
+ * bounded wait inside a kernel gave up (the kernel then stops early and its
+ * outputs are not valid).  Synchronises the device; `reset` != 0 clears the
+ * word.  Not for use inside graph capture.
+ */
+int ar_device_status(int device, int reset);
+
+/*
+ * Launch, on `device`, a kernel whose only work is a wait on an mbarrier
+ * that nothing completes, bounded by limit_us microseconds, and return what
+ * the status word then holds (AR_ERR_TIMEOUT expected) after clearing it.
+ * Checks the bounded-wait path without faulting or hanging the GPU.
+ */
+int ar_selftest_bounded_wait(int device, unsigned limit_us);
 
 /* A short English description of a status code (static storage). */
 const char *ar_strerror(int status);

@@ -138,21 +138,37 @@ SHAPES = [(2, 4, 1024), (8, 1, 7168), (8, 16, 7168), (4, 32, 7168), (4, 2048, 71
 def test_plan_covers_every_pack(arlib, n, m, H, mode):
     p = arlib.ar_get_plan(n, m, H, mode, sm_count=152)
     P = H // 8
-    per_cta = -(-P // p["cluster"])
     assert p["mode"] in (1, 2) and (mode == 0 or p["mode"] == mode)
-    assert p["cluster"] in (1, 2, 4, 8, 16) and p["vpt"] in (1, 2, 4, 8)
-    assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024 // p["vpt"]
-    assert p["threads"] * p["vpt"] >= per_cta          # every pack has an owner
-    assert per_cta <= 1024                             # a CTA holds its row slice in registers
-    assert p["ctas"] == m * p["cluster"]
     assert p["launches"] == (2 if p["mode"] == 2 else 1)
+    assert p["vpt"] in (1, 2, 4, 8)
+    if p["kernel"] == 1:   # register kernel: one CTA or a cluster per row
+        per_cta = -(-P // p["cluster"])
+        assert p["cluster"] in (1, 2, 4, 8, 16) and p["stages"] == 0
+        assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024 // p["vpt"]
+        assert p["threads"] * p["vpt"] >= per_cta          # every pack has an owner
+        assert per_cta <= 1024                             # a row slice fits in registers
+        assert p["ctas"] == m * p["cluster"]
+    else:                  # stream kernel: persistent, producer warp + consumers
+        assert p["kernel"] == 2 and p["cluster"] == 1
+        tc = p["threads"] - 32
+        assert tc % 32 == 0 and 32 <= tc <= 512
+        tiles = -(-P // tc)
+        assert tiles <= p["vpt"]                           # the template holds every tile
+        inputs = n if p["mode"] == 1 else 1
+        smem = p["stages"] * (inputs + 1) * tc * 16 + 16 * p["stages"] + 256 + 16
+        assert 2 <= p["stages"] <= 16 and smem <= 232448
+        assert p["ctas"] == min(m, 152)
 
 
 def test_plan_spreads_small_batches(arlib):
     # decode: a single row of H = 7168 spreads over a 16-CTA cluster
     assert arlib.ar_get_plan(8, 1, 7168, 1, sm_count=152)["cluster"] == 16
-    # prefill: rows alone fill the GPU; one CTA per row
-    assert arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)["cluster"] == 1
+    # prefill: rows alone fill the GPU; one persistent streaming CTA per SM
+    p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
+    assert p["kernel"] == 2 and p["ctas"] == 152
+    # H above the stream kernel's limit: the register kernel with a cluster
+    p = arlib.ar_get_plan(3, 1000, 65536, 1, sm_count=152)
+    assert p["kernel"] == 1 and p["cluster"] == 8
 
 
 def test_plan_rejects_bad_shapes(arlib):

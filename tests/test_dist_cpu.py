@@ -1,0 +1,74 @@
+"""The bench's multi-rank host logic on CPU ranks (gloo, world size 2):
+barrier, max and sum over ranks, and the rank-0-only reference arm under
+torchrun.  No GPU is involved."""
+import json
+import multiprocessing as mp
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), ARN_DIST_BACKEND="gloo")
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    import bench
+    w, r, _ = bench.dist_setup(None)
+    bench.barrier(w)
+    mx = bench.max_over_ranks(w, 10.0 * (r + 1))
+    sm = bench.sum_over_ranks(w, 10.0 * (r + 1))
+    bench.barrier(w)
+    q.put((r, w, mx, sm))
+    dist.destroy_process_group()
+
+
+def test_max_and_sum_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert got == [(0, 2, 20.0, 30.0), (1, 2, 20.0, 30.0)]
+
+
+def test_single_rank_needs_no_process_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.max_over_ranks(1, 3.5) == 3.5
+    assert bench.sum_over_ranks(1, 3.5) == 3.5
+    bench.barrier(1)
+
+
+@pytest.mark.slow
+def test_reference_arm_under_torchrun_prints_one_line():
+    port = free_port()
+    env = dict(os.environ, OMP_NUM_THREADS="1")
+    r = subprocess.run(
+        [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+         "--master-addr", "127.0.0.1", "--master-port", str(port), "bench.py", "--impl",
+         "reference", "--gpus", "2", "--steps", "3", "--warmup", "3", "--quick"],
+        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0

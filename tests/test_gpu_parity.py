@@ -224,6 +224,47 @@ def test_large_and_small_magnitudes_and_zero_rows(scale):
     check_full(inp, "two_stage", "large magnitudes two-stage")
 
 
+# ------------------------------------------------------------------ kernels
+
+STREAM_CASES = [(8, 8192, 6144), (4, 2048, 7168), (8, 300, 8192), (1, 7, 1032), (3, 151, 7176),
+                (16, 40, 4096), (2, 1000, 24), (5, 64, 16384), (8, 19, 32768), (12, 500, 2048)]
+
+
+@pytest.mark.parametrize("n,m,H", STREAM_CASES)
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_stream_kernel_against_oracle_and_register_kernel(n, m, H, mode):
+    w = synth.Workload("stream", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=m + H)
+    inp = device_inputs(w, m)
+    a = run_gpu(inp, mode, kernel="stream")
+    b = run_gpu(inp, mode, kernel="register")
+    torch.cuda.synchronize()
+    assert torch.equal(a[2].view(torch.int32), b[2].view(torch.int32))
+    assert torch.equal(a[1].view(torch.int16), b[1].view(torch.int16))
+    rows = sample_rows(m, 64)
+    idx = torch.as_tensor(rows, device="cuda")
+    compare((a[0][idx], a[1][idx], a[2][idx]), oracle_rows(inp, rows, mode == "two_stage"),
+            f"stream n={n} m={m} H={H}/{mode}")
+    assert arn.ar_device_status(0) == arn.AR_OK
+
+
+@pytest.mark.parametrize("n", range(1, 17))
+def test_stream_kernel_every_rank_count(n):
+    w = synth.Workload("stream_ranks", n=n, H=7168, ms=(33,), p_std=0.5, res_std=1.0, seed=n)
+    check_full(device_inputs(w, 33), "one_stage", f"stream n={n}", kernel="stream")
+
+
+def test_stream_kernel_order_sensitive():
+    inp = wide_range_inputs(8, 320, 6144, seed=3)
+    check_full(inp, "one_stage", "stream order-sensitive", kernel="stream")
+
+
+def test_bounded_wait_gives_up_and_reports():
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    assert arn.ar_selftest_bounded_wait(0, 2000) == arn.AR_ERR_TIMEOUT
+    assert arn.ar_device_status(0) == arn.AR_OK      # the self-test clears it
+    check_full(device_inputs(synth.TINY, 4), "one_stage", "after the self-test")
+
+
 # ------------------------------------------------------------------ stages
 
 def test_stage_entry_points():
