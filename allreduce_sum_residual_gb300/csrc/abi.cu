@@ -278,22 +278,32 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   return AR_OK;
 }
 
+// `after_prior`: launch with a programmatic dependency on the previous grid
+// in the stream (stage 2 after stage 1): the kernel may start while that
+// grid drains and waits for it with griddepcontrol.wait.
 static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t &pl,
-                                   cudaStream_t stream) {
+                                   bool after_prior, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  int na = 0;
   if (pl.cluster > 1) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = static_cast<unsigned>(pl.cluster);
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
   }
+  if (after_prior) {
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = na ? attr : nullptr;
+  cfg.numAttrs = na;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt), a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -302,7 +312,7 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
 static cudaError_t launch_stream(const void *const *inputs, int n, const void *residual,
                                  const void *weight, float eps, int64_t m, int64_t H, void *out,
                                  void *residual_out, float *sum_out, const ar_plan_t &pl,
-                                 int *status, cudaStream_t stream) {
+                                 int *status, bool after_prior, cudaStream_t stream) {
   StreamArgs a;
   std::memset(&a, 0, sizeof a);
   for (int k = 0; k < n; ++k) a.src[k] = static_cast<const uint4 *>(inputs[k]);
@@ -320,8 +330,20 @@ static cudaError_t launch_stream(const void *const *inputs, int n, const void *r
   a.eps = eps;
   a.wait_limit_ns = kWaitLimitNs;
   a.status = status;
-  const size_t smem = static_cast<size_t>(stream_smem_bytes(n, Tc, pl.stages));
-  stream_kernel(n, pl.vpt)<<<static_cast<unsigned>(pl.ctas), pl.threads, smem, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
+  cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
+  cfg.dynamicSmemBytes = static_cast<size_t>(stream_smem_bytes(n, Tc, pl.stages));
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  if (after_prior) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel(n, pl.vpt), a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 
@@ -360,20 +382,20 @@ static int run(const void *const *partials, int n, const void *residual, const v
   if (st != AR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The epilogue over `inputs` (the partials, or the two-stage temporary).
-  auto epilogue = [&](const void *const *inputs, int count) -> int {
+  auto epilogue = [&](const void *const *inputs, int count, bool after_prior) -> int {
     cudaError_t e;
     if (pl.kernel == AR_KERNEL_STREAM) {
       e = launch_stream(inputs, count, residual, weight, eps, m, H, out, residual_out, sum_out, pl,
-                        d->status, s);
+                        d->status, after_prior, s);
     } else {
       EpilogueArgs a;
       fill_epilogue_args(&a, inputs, count, residual, weight, eps, m, H, out, residual_out,
                          sum_out, pl);
-      e = launch_epilogue(a, count, pl, s);
+      e = launch_epilogue(a, count, pl, after_prior, s);
     }
     return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
   };
-  if (pl.mode == AR_MODE_ONE_STAGE) return epilogue(partials, n);
+  if (pl.mode == AR_MODE_ONE_STAGE) return epilogue(partials, n, false);
   // two-stage: stage 1 into the workspace, stage 2 from it
   void *ws;
   {
@@ -396,7 +418,7 @@ static int run(const void *const *partials, int n, const void *residual, const v
   ra.npacks = m * H / kPackElems;
   if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   const void *temp_in[1] = {ws};
-  return epilogue(temp_in, 1);
+  return epilogue(temp_in, 1, true);
 }
 
 }  // namespace arn

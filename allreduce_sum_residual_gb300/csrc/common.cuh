@@ -96,6 +96,21 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
   return scratch[32];
 }
 
+// --- programmatic dependent launch ---------------------------------------------------
+
+// Let the next kernel in the stream (launched with programmatic stream
+// serialization) start its prologue while this grid finishes.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Wait until the preceding grid in the stream has completed and its writes
+// are visible.  Returns at once when this grid was launched without a
+// programmatic dependency.
+__device__ __forceinline__ void pdl_wait_prior_grid() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --- thread-block clusters --------------------------------------------------------
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -55,17 +55,28 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   const int T = blockDim.x;
 
   // Loads first: n partials, the residual and the weight of every pack this
-  // thread owns.  Nothing is stored before the last load is issued.
+  // thread owns.  Nothing is stored before the last load is issued.  The
+  // weight and the residual come from before the previous grid in the
+  // stream, so they are read before waiting on it (stage 2 launched with a
+  // programmatic dependency on stage 1); the partials only after.
   float r[VPT][8];
-  uint4 wv[VPT];
+  uint4 wv[VPT], rv[VPT];
+#pragma unroll
+  for (int v = 0; v < VPT; ++v) {
+    const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
+    if (c < c1) {
+      wv[v] = ld_ro(a.w + c);
+      rv[v] = ld_ro(a.res + base + c);
+    }
+  }
+  pdl_wait_prior_grid();
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
     if (c < c1) {
       float acc[8], rs[8];
       sum_pack_in_rank_order<N>(a.p, base + c, acc);
-      unpack8(ld_ro(a.res + base + c), rs);
-      wv[v] = ld_ro(a.w + c);
+      unpack8(rv[v], rs);
       if (a.sum != nullptr) {
         a.sum[2 * (base + c)] = make_float4(acc[0], acc[1], acc[2], acc[3]);
         a.sum[2 * (base + c) + 1] = make_float4(acc[4], acc[5], acc[6], acc[7]);

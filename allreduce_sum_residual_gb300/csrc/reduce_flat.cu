@@ -20,6 +20,9 @@ constexpr int kReduceThreads = 256;
 template <int N, int U>
 __global__ void __launch_bounds__(kReduceThreads)
 k_reduce_flat(const __grid_constant__ ReduceArgs a) {
+  // Stage 2 may be scheduled as soon as SMs free up; it waits for this
+  // grid's results itself (griddepcontrol.wait) before reading them.
+  pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads * U;
   for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kReduceThreads * U + threadIdx.x;
        i0 < a.npacks; i0 += stride) {

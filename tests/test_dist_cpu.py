@@ -72,3 +72,55 @@ def test_reference_arm_under_torchrun_prints_one_line():
     assert d["impl"] == "reference" and d["n_gpus"] == 2 and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle"
     assert d["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def _consensus_rank(rank, world, port, fail_rank, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from allreduce_sum_residual_gb300 import consensus
+    dist.init_process_group("gloo")
+    held = []
+
+    def reserve(elems, device):
+        if rank == fail_rank:
+            raise MemoryError("injected rank-local allocation failure")
+        held.append(elems)
+
+    def release(device):
+        held.clear()
+
+    ok = consensus.reserve_two_stage_workspace(1 << 20, rank, reserve=reserve, release=release)
+    # every rank then takes the same path; a collective after the decision
+    # completes on all ranks (no split between two different collectives)
+    dist.barrier()
+    q.put((rank, ok, list(held)))
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("fail_rank", [None, 0, 1])
+def test_decline_is_collective(fail_rank):
+    """An allocation failure injected on one rank makes every rank decline
+    the two-stage path and hold no workspace; without a failure every rank
+    keeps it."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_consensus_rank, args=(r, 2, port, fail_rank, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    if fail_rank is None:
+        assert got == [(0, True, [1 << 20]), (1, True, [1 << 20])]
+    else:
+        assert got == [(0, False, []), (1, False, [])]
+
+
+def test_agree_without_a_process_group():
+    sys.path.insert(0, ROOT)
+    from allreduce_sum_residual_gb300 import consensus
+    assert consensus.agree(True) is True and consensus.agree(False) is False
