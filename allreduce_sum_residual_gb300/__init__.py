@@ -29,6 +29,8 @@ AR_ERR_WORKSPACE = 4
 AR_ERR_CUDA = 5
 AR_ERR_TIMEOUT = 6
 AR_ERR_UNSUPPORTED = 7
+AR_ERR_SCRATCH_LIMIT = 8
+AR_STATIC_SCRATCH_ELEMS = 8 * 1024 * 1024
 
 AR_MODE_AUTO = 0
 AR_MODE_ONE_STAGE = 1
@@ -77,6 +79,8 @@ _SIGS = {
     "ar_release_workspace": (ctypes.c_int, [ctypes.c_int]),
     "ar_workspace_elems": (_I64, [ctypes.c_int]),
     "ar_select_mode": (ctypes.c_int, [ctypes.c_int, _I64, _I64]),
+    "ar_rmsnorm_two_stage_static": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP,
+                                                   ctypes.c_float, _I64, _I64, _VP, _VP, _VP]),
     "ar_device_status": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "ar_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint]),
     "ar_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -198,6 +202,20 @@ def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
                              _VP(sum_out.data_ptr()) if sum_out is not None else None, plan)
     _check(st, "ar_rmsnorm_ex")
     return out, residual_out, sum_out
+
+
+def ar_rmsnorm_two_stage_static(partials, residual, weight, eps, out=None, residual_out=None,
+                                stream=None):
+    """Two-stage epilogue that allocates no device memory: its temporary is a
+    fixed 16 MiB array inside the library (m * H <= AR_STATIC_SCRATCH_ELEMS).
+    For callers that may not call cudaMalloc; calls share that array, so
+    calls overlapping on the GPU race.  Returns (out, residual_out)."""
+    m, H, dev, out, residual_out, arr = _prepare(partials, residual, weight, out, residual_out)
+    st = lib().ar_rmsnorm_two_stage_static(arr, len(partials), _ptr(residual), _ptr(weight),
+                                           float(eps), m, H, _ptr(out), _ptr(residual_out),
+                                           _stream_ptr(stream, dev))
+    _check(st, "ar_rmsnorm_two_stage_static")
+    return out, residual_out
 
 
 def ar_reduce_scatter_flat(partials, temp, stream=None):

@@ -421,6 +421,50 @@ static int run(const void *const *partials, int n, const void *residual, const v
   return epilogue(temp_in, 1, true);
 }
 
+// The two-stage path with a temporary the caller supplies (`temp`, room for
+// `temp_elems` bf16), instead of the reserved workspace.  Same checks, plan
+// and kernels as ar_rmsnorm in AR_MODE_TWO_STAGE; allocates nothing.
+int two_stage_with_temp(const void *const *partials, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, void *temp, int64_t temp_elems, void *stream) {
+  int st = check_shape(n, m, H, eps);
+  if (st != AR_OK) return st;
+  if (m == 0) return AR_OK;
+  st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, nullptr);
+  if (st != AR_OK) return st;
+  if (!temp || !aligned16(temp) || temp_elems < m * H) return AR_ERR_ARG;
+  const int64_t bytes = m * H * 2;
+  const Range tr = range_of(temp, bytes);
+  if (overlap(tr, range_of(out, bytes)) || overlap(tr, range_of(residual_out, bytes)) ||
+      overlap(tr, range_of(residual, bytes)) || overlap(tr, range_of(weight, H * 2)))
+    return AR_ERR_ALIAS;
+  for (int k = 0; k < n; ++k)
+    if (overlap(tr, range_of(partials[k], bytes))) return AR_ERR_ALIAS;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  ar_plan_t pl;
+  st = make_plan(n, m, H, AR_MODE_TWO_STAGE, d->sms, d->smem_optin, nullptr, &pl);
+  if (st != AR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ReduceArgs ra;
+  std::memset(&ra, 0, sizeof ra);
+  for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
+  ra.temp = static_cast<uint4 *>(temp);
+  ra.npacks = m * H / kPackElems;
+  if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
+  const void *temp_in[1] = {temp};
+  cudaError_t e;
+  if (pl.kernel == AR_KERNEL_STREAM) {
+    e = launch_stream(temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                      d->status, true, s);
+  } else {
+    EpilogueArgs a;
+    fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl);
+    e = launch_epilogue(a, 1, pl, true, s);
+  }
+  return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+}
+
 }  // namespace arn
 
 using namespace arn;
@@ -611,6 +655,8 @@ const char *ar_strerror(int status) {
     case AR_ERR_CUDA: return "CUDA runtime error or launch failure";
     case AR_ERR_TIMEOUT: return "a bounded device-side wait timed out";
     case AR_ERR_UNSUPPORTED: return "unsupported size (H above AR_MAX_HIDDEN or too many rows)";
+    case AR_ERR_SCRATCH_LIMIT:
+      return "m*H exceeds the fixed device scratch of ar_rmsnorm_two_stage_static (AR_STATIC_SCRATCH_ELEMS)";
     default: return "unknown status";
   }
 }

@@ -76,6 +76,8 @@ extern "C" {
 #define AR_ERR_CUDA        5  /* a CUDA runtime call or a launch failed        */
 #define AR_ERR_TIMEOUT     6  /* a bounded device-side wait ran out            */
 #define AR_ERR_UNSUPPORTED 7  /* H above AR_MAX_HIDDEN                         */
+#define AR_ERR_SCRATCH_LIMIT 8 /* m*H above AR_STATIC_SCRATCH_ELEMS
+                                  (ar_rmsnorm_two_stage_static only)          */
 
 /* Modes. */
 #define AR_MODE_AUTO       0  /* pick by ar_select_mode(n, m, H)               */
@@ -176,6 +178,42 @@ int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count,
 int ar_load_rmsnorm(const void *temp, const void *residual, const void *weight,
                     float eps, int64_t m, int64_t H, void *out,
                     void *residual_out, void *stream);
+
+/*
+ * Two-stage epilogue for callers that cannot allocate device memory.
+ * (The pages have no counterpart of this entry point; it belongs to this
+ * library's API only.)
+ *
+ * Who needs it: code that may not call cudaMalloc -- for example a plug-in
+ * inside a host program that owns all device memory through its own pool
+ * and forbids other allocations, a process whose memory is already fully
+ * reserved by a framework's caching allocator, or a latency-critical path
+ * that cannot accept the implicit device synchronisation cudaMalloc and
+ * cudaFree may cause.  ar_rmsnorm's two-stage path needs a workspace from
+ * ar_reserve_workspace (a cudaMalloc); this one does not.
+ *
+ * The bf16 temporary lives in a fixed array of AR_STATIC_SCRATCH_ELEMS
+ * elements (16 MiB) compiled into the library as device memory: every GPU
+ * that loads the library holds it until the process exits.  Arguments,
+ * layout and results are those of ar_rmsnorm with AR_MODE_TWO_STAGE.
+ *   - m*H above AR_STATIC_SCRATCH_ELEMS returns AR_ERR_SCRATCH_LIMIT and
+ *     launches nothing.
+ *   - Nothing is allocated: no cudaMalloc, no cudaFree, no allocating
+ *     library routine.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the previous call's
+ *     contents.  Nothing in it has to start at zero (stage 1 overwrites the
+ *     m*H elements stage 2 reads), but calls that overlap on the GPU (on
+ *     different streams, or from different host threads without ordering)
+ *     race on it: order them, e.g. on one stream.
+ */
+#define AR_STATIC_SCRATCH_ELEMS (8ll * 1024 * 1024)
+int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
+                                const void *residual, const void *weight,
+                                float eps, int64_t m, int64_t H, void *out,
+                                void *residual_out, void *stream);
 
 /*
  * Reserve the two-stage workspace (max_elems bf16 elements, i.e. the largest
