@@ -285,9 +285,11 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   return AR_OK;
 }
 
-// `after_prior`: launch with a programmatic dependency on the previous grid
-// in the stream (stage 2 after stage 1): the kernel may start while that
-// grid drains and waits for it with griddepcontrol.wait.
+// Every launch carries programmatic stream serialization: the kernel may be
+// scheduled while the previous grid in the stream drains, and waits for it
+// (griddepcontrol.wait) before touching global memory.  `after_prior` marks
+// stage 2, whose predecessor is stage 1 of the same call: it may read the
+// weight and the residual before that wait.
 static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t &pl,
                                    bool after_prior, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -304,14 +306,14 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
-  if (after_prior) {
-    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[na].val.programmaticStreamSerializationAllowed = 1;
-    ++na;
-  }
-  cfg.attrs = na ? attr : nullptr;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  cfg.attrs = attr;
   cfg.numAttrs = na;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt), a);
+  EpilogueArgs args = a;
+  args.early_reads = after_prior ? 1 : 0;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt), args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -342,13 +344,12 @@ static cudaError_t launch_stream(const void *const *inputs, int n, const void *r
   cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(stream_smem_bytes(n, Tc, pl.stages));
   cfg.stream = stream;
+  (void)after_prior;  // the stream kernel waits on the previous grid before any global access
   cudaLaunchAttribute attr[1];
-  if (after_prior) {
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-  }
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   const cudaError_t e = cudaLaunchKernelEx(&cfg, stream_kernel(n, pl.vpt), a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -29,6 +29,8 @@ struct EpilogueArgs {
   int per_cta;                   // packs of a row one CTA covers
   float H;                       // columns, as the divisor of the mean
   float eps;
+  int early_reads;               // weight and residual may be read before the
+                                 // wait on the previous grid (stage 2 only)
 };
 
 // Kernel parameters of stage 1 (flat reduce of every pack across ranks).
@@ -97,16 +99,23 @@ __device__ __forceinline__ float block_sum(float v, float *scratch) {
 }
 
 // --- programmatic dependent launch ---------------------------------------------------
+//
+// Every kernel of the library is launched with programmatic stream
+// serialization, so it may be scheduled before the previous grid in the
+// stream has finished.  Each kernel therefore (1) waits for the previous
+// grids (griddepcontrol.wait) before it reads or writes global memory --
+// which keeps plain stream-order semantics whatever ran before -- and only
+// then (2) allows the next kernel to be scheduled.  Because of that order,
+// when a kernel starts every grid before its predecessor has completed.
 
-// Let the next kernel in the stream (launched with programmatic stream
-// serialization) start its prologue while this grid finishes.
+// Let the next kernel in the stream start its prologue while this grid runs.
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// Wait until the preceding grid in the stream has completed and its writes
-// are visible.  Returns at once when this grid was launched without a
-// programmatic dependency.
+// Wait until the preceding grids in the stream have completed and their
+// writes are visible.  Returns at once when this grid was launched without
+// a programmatic dependency.
 __device__ __forceinline__ void pdl_wait_prior_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }

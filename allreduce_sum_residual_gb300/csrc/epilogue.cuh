@@ -55,12 +55,13 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   const int T = blockDim.x;
 
   // Loads first: n partials, the residual and the weight of every pack this
-  // thread owns.  Nothing is stored before the last load is issued.  The
-  // weight and the residual come from before the previous grid in the
-  // stream, so they are read before waiting on it (stage 2 launched with a
-  // programmatic dependency on stage 1); the partials only after.
+  // thread owns.  Nothing is stored before the last load is issued.  In
+  // stage 2 the previous grid is stage 1, which writes neither the weight
+  // nor the residual (and everything before stage 1 has completed), so
+  // those two are read before the wait; the temporary only after.
   float r[VPT][8];
   uint4 wv[VPT], rv[VPT];
+  if (!a.early_reads) pdl_wait_prior_grid();
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
@@ -69,7 +70,8 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
       rv[v] = ld_ro(a.res + base + c);
     }
   }
-  pdl_wait_prior_grid();
+  if (a.early_reads) pdl_wait_prior_grid();
+  pdl_launch_dependents();
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;

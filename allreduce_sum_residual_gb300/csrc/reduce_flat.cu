@@ -20,8 +20,9 @@ constexpr int kReduceThreads = 256;
 template <int N, int U>
 __global__ void __launch_bounds__(kReduceThreads)
 k_reduce_flat(const __grid_constant__ ReduceArgs a) {
-  // Stage 2 may be scheduled as soon as SMs free up; it waits for this
-  // grid's results itself (griddepcontrol.wait) before reading them.
+  // Previous grids first, then let stage 2 be scheduled; stage 2 waits for
+  // this grid's results itself (griddepcontrol.wait) before reading them.
+  pdl_wait_prior_grid();
   pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads * U;
   for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kReduceThreads * U + threadIdx.x;
@@ -60,7 +61,17 @@ cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t
   const int64_t cap = static_cast<int64_t>(sms) * (2048 / kReduceThreads);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  reduce_kernel(n)<<<static_cast<unsigned>(blocks), kReduceThreads, 0, stream>>>(a);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(blocks), 1, 1);
+  cfg.blockDim = dim3(kReduceThreads, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, reduce_kernel(n), a);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -151,6 +151,8 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_wait_prior_grid();
+  pdl_launch_dependents();
 
   const int64_t G = gridDim.x;
   const int V = a.tiles;
@@ -158,8 +160,6 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
   if (warp == 0) {
     // ---------------- producer
     if (lane != 0) return;
-    // Stage 2 reads the temporary that the previous grid (stage 1) writes.
-    pdl_wait_prior_grid();
     int64_t t = 0;
     for (int64_t row = blockIdx.x; row < a.m; row += G) {
       for (int v = 0; v < V; ++v, ++t) {

@@ -58,10 +58,18 @@ def peaks():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def source_hash():
+KERNEL_SOURCES = {
+    "k_stream_epilogue": ("common.cuh", "stream_epilogue.cuh"),
+    "k_fused_epilogue": ("common.cuh", "epilogue.cuh"),
+    "k_reduce_flat": ("common.cuh", "epilogue.cuh", "reduce_flat.cu"),
+}
+
+
+def source_hash(kernel):
+    """Hash of the files that define `kernel` (its device code)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "allreduce_sum_residual_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -75,7 +83,7 @@ def ncu_traffic(kernel, workload):
         with open(path) as f:
             d = json.load(f)
         e = d[f"{kernel}@{workload}"]
-        if e.get("source_hash") != source_hash():
+        if e.get("source_hash") != source_hash(kernel):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -186,30 +194,48 @@ def sum_over_ranks(world, x, device=None):
 
 # ---------------------------------------------------------------- our arm
 
-def timed_steps(fn, stream, steps, warmup, world, device):
-    """W warm-up steps, then K steps timed with CUDA events on `stream`,
-    bracketed by barrier + synchronize; returns (total_s, per-step list)."""
+def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=100):
+    """W warm-up steps, then exactly K steps timed with CUDA events on
+    `stream`, bracketed by barrier + synchronize.  With `use_graph` the K
+    steps are replayed from CUDA graphs of `chunk` steps (plus one graph for
+    the remainder), so host launch overhead stays out of the timed region,
+    as in the pages' method.  Returns (total_s, mean step s)."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(device)
+    graphs = []
+    if use_graph:
+        full, rest = divmod(steps, chunk)
+        for count in ([chunk] if full else []) + ([rest] if rest else []):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for _ in range(count):
+                    fn()
+            graphs.append((g, count))
+        plan = [graphs[0]] * full + ([graphs[-1]] if rest else []) if full else graphs
+        with torch.cuda.stream(stream):
+            for g, _ in graphs:   # one untimed replay of each graph
+                g.replay()
+        torch.cuda.synchronize(device)
     barrier(world, device)
     torch.cuda.synchronize(device)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for a, b in ev:
-        a.record(stream)
-        fn()
-        b.record(stream)
+    if use_graph:
+        with torch.cuda.stream(stream):
+            for g, _ in plan:
+                g.replay()
+    else:
+        for _ in range(steps):
+            fn()
     t1.record(stream)
     torch.cuda.synchronize(device)
     barrier(world, device)
     total = t0.elapsed_time(t1) / 1e3
-    per = [a.elapsed_time(b) / 1e3 for a, b in ev]
-    return total, per
+    del graphs
+    return total, total / steps
 
 
 def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80):
@@ -376,13 +402,12 @@ def run_ours(args):
                                   residual_out=rout, mode=step_mode, kernel=args.kernel)
 
     with ClockSampler(local) as clk:
-        total, per = timed_steps(step, stream, args.steps, args.warmup, world, device)
+        total, mean_step = timed_steps(step, stream, args.steps, args.warmup, world, device,
+                                       use_graph=not args.eager)
     clocks = clk.summary()
     total_max = max_over_ranks(world, total, device)
     bytes_step = algo_bytes(n, m, H)
     value = sum_over_ranks(world, bytes_step * args.steps, device) / total_max / 1e9
-    mean_step = statistics.mean(per)
-    best_step = min(per)
 
     # the other path on the same shape (both are timed for prefill)
     other = "two_stage" if path == "one_stage" else "one_stage"
@@ -392,16 +417,14 @@ def run_ours(args):
             arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, inp.eps, out=out,
                            residual_out=rout, mode=other)
 
-    per_o = per
+    mean_o = mean_step
     if not args.kernel_only:
-        _, per_o = timed_steps(step_other, stream, max(10, min(args.steps, 200)), 3, 1, device)
-    modes = {path: {"us_mean": round(mean_step * 1e6, 2), "us_min": round(best_step * 1e6, 2),
-                    "gbs": round(bytes_step / mean_step / 1e9, 1)},
-             other: {"us_mean": round(statistics.mean(per_o) * 1e6, 2),
-                     "us_min": round(min(per_o) * 1e6, 2),
-                     "gbs": round(bytes_step / statistics.mean(per_o) / 1e9, 1),
+        _, mean_o = timed_steps(step_other, stream, max(10, min(args.steps, 500)), 3, 1, device,
+                                use_graph=not args.eager)
+    modes = {path: {"us": round(mean_step * 1e6, 2), "gbs": round(bytes_step / mean_step / 1e9, 1)},
+             other: {"us": round(mean_o * 1e6, 2), "gbs": round(bytes_step / mean_o / 1e9, 1),
                      "gbs_actual_bytes": round(actual_bytes(n, m, H, other == "two_stage")
-                                               / statistics.mean(per_o) / 1e9, 1)}}
+                                               / mean_o / 1e9, 1)}}
 
     peak, peak_kind = peaks()
     kernel = ("k_reduce_flat" if path == "two_stage" else
@@ -441,7 +464,9 @@ def run_ours(args):
                        "plan": plan, "l2": f"inputs {bytes_step / 1e9:.2f} GB > L2 "
                                            f"{l2 / 2**20:.0f} MiB; no flush needed",
                        "parallelism": f"replicas x{world}",
-                       "timing": "CUDA events per step on the launch stream, max over ranks"},
+                       "timing": ("CUDA events around K steps replayed from CUDA graphs on the launch "
+                       "stream" if not args.eager else "CUDA events around K eager steps")
+                      + ", max over ranks"},
             "pct_of_8tbs": round(value / world / 8000.0 * 100, 2),
             "roofline": roofline, "modes": modes,
             "cpu_baseline": cpu,
@@ -551,6 +576,8 @@ def main(argv=None):
     ap.add_argument("--mode", default="auto", choices=("auto", "one_stage", "two_stage"))
     ap.add_argument("--kernel", default="auto", choices=("auto", "register", "stream"),
                     help="force the epilogue kernel (profiling)")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one by one from Python instead of from graphs")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only the timed steps (no latency table, e2e or CPU baseline)")
     args = ap.parse_args(argv)
