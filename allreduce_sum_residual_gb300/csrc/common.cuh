@@ -134,22 +134,31 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return r;
 }
 
-// Cluster-wide barrier; release/acquire order shared-memory writes before it
-// against distributed-shared-memory reads after it.
+// Cluster-wide barrier; release/acquire order the distributed-shared-memory
+// writes before it against the reads after it.
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n"
                "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Read a float from the shared memory of CTA `rank` of this cluster, at the
+// Split phase of the cluster barrier with no memory ordering: arrive at the
+// start of the kernel, wait right before the first access to a peer's shared
+// memory -- which must not happen before every CTA of the cluster runs.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+}
+
+// Write a float into the shared memory of CTA `rank` of this cluster, at the
 // address that `local` has in this CTA.
-__device__ __forceinline__ float ld_dsmem(const float *local, uint32_t rank) {
+__device__ __forceinline__ void st_dsmem(float *local, uint32_t rank, float v) {
   uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
   uint32_t remote;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-  return v;
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
 }
 
 }  // namespace arn

@@ -12,9 +12,12 @@
 // bytes.  Every partial element is owned by exactly one thread, which sums
 // it over the ranks in order: the sum does not depend on S, T or VPT.
 //
-// The square sum is reduced warp -> CTA -> cluster; the cluster step reads
-// each CTA's total from distributed shared memory in rank order, so every
-// CTA of a row derives the same scale.
+// The square sum is reduced warp -> CTA -> cluster.  In the cluster step
+// every CTA writes its total into slot q of every peer's shared memory
+// (distributed shared memory), one cluster barrier publishes the writes,
+// and each CTA adds slots 0..S-1 in rank order: all CTAs of a row derive
+// the same scale, and no CTA touches a peer's memory after the barrier, so
+// none has to wait for the others before it exits.
 #pragma once
 
 #include "common.cuh"
@@ -44,7 +47,7 @@ template <int N, int VPT>
 __global__ void __launch_bounds__(1024 / VPT)
 k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   __shared__ float red[33];
-  __shared__ float cta_total;
+  __shared__ float cta_totals[kMaxClusterCtas];
 
   const uint32_t S = cluster_nctarank();       // 1 unless launched as a cluster
   const uint32_t q = cluster_ctarank();
@@ -53,6 +56,7 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   const int c1 = min(a.P, c0 + a.per_cta);
   const int64_t base = row * static_cast<int64_t>(a.P);
   const int T = blockDim.x;
+  if (S > 1) cluster_arrive_relaxed();  // this CTA runs (see the cluster step)
 
   // Loads first: n partials, the residual and the weight of every pack this
   // thread owns.  Nothing is stored before the last load is issued.  In
@@ -104,10 +108,11 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
 
   float total = block_sum(ss, red);
   if (S > 1) {
-    if (threadIdx.x == 0) cta_total = total;
+    cluster_wait();  // every CTA of the cluster has started: peers' memory is live
+    if (threadIdx.x < S) st_dsmem(&cta_totals[q], threadIdx.x, total);
     cluster_sync();
     total = 0.f;
-    for (uint32_t k = 0; k < S; ++k) total += ld_dsmem(&cta_total, k);
+    for (uint32_t k = 0; k < S; ++k) total += cta_totals[k];
   }
   const float inv = rsqrtf(total / a.H + a.eps);
 
@@ -122,9 +127,6 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
       st_stream(a.out + base + c, pack8(y));
     }
   }
-
-  // No CTA may leave while a peer can still read its cta_total.
-  if (S > 1) cluster_sync();
 }
 
 // Kernel pointer for (n, vpt); n in [1, AR_MAX_RANKS], vpt in {1, 2, 4, 8}.

@@ -152,7 +152,6 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
   }
   __syncthreads();
   pdl_wait_prior_grid();
-  pdl_launch_dependents();
 
   const int64_t G = gridDim.x;
   const int V = a.tiles;
@@ -179,6 +178,9 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
         for (int j = 0; j <= N; ++j) bulk_g2s(dst + static_cast<size_t>(j) * Tc, a.src[j] + off, bytes, &full[s]);
       }
     }
+    // This CTA is near its end: the next grid may be scheduled.  (Released
+    // late, so that its CTAs do not sit on these SMs while the ring runs.)
+    pdl_launch_dependents();
   drain:
     // Every slot's last issued fill must land before the CTA may exit.
     for (int s = 0; s < S; ++s) {
@@ -208,6 +210,7 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
   int parity_row = 0;
   for (int64_t row = blockIdx.x; row < a.m; row += G, parity_row ^= 1) {
     const int64_t base = row * a.P;
+    if (row + G >= a.m) pdl_launch_dependents();  // last row of this CTA
     float r[VPT][8];
     float ss = 0.f;
 #pragma unroll

@@ -238,21 +238,30 @@ def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=
     return total, total / steps
 
 
-def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80):
+def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=None):
     """The pages' method: `calls` calls in one CUDA graph (cycling over the
-    input sets in `inps`), per-call time = min over replays / calls."""
+    input sets in `inps`), per-call time = min over replays / calls.
+    `shape` = (kernel, cluster, vpt) forces a launch shape."""
     import torch
     outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
+
+    def call(i, o, r):
+        if shape is None:
+            arn.ar_rmsnorm(i.partials, i.residual, i.weight, eps, out=o, residual_out=r, mode=mode)
+        else:
+            arn.ar_rmsnorm_ex(i.partials, i.residual, i.weight, eps, out=o, residual_out=r,
+                              mode=mode, kernel=shape[0], cluster=shape[1], vpt=shape[2])
+
     with torch.cuda.stream(stream):
         for i, (o, r) in zip(inps, outs):
-            arn.ar_rmsnorm(i.partials, i.residual, i.weight, eps, out=o, residual_out=r, mode=mode)
+            call(i, o, r)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for c in range(calls):
             i = inps[c % len(inps)]
             o, r = outs[c % len(outs)]
-            arn.ar_rmsnorm(i.partials, i.residual, i.weight, eps, out=o, residual_out=r, mode=mode)
+            call(i, o, r)
     best = float("inf")
     with torch.cuda.stream(stream):
         g.replay()
@@ -562,6 +571,42 @@ def run_sweep(args):
             torch.cuda.empty_cache()
 
 
+def run_shapes(args):
+    """Register-kernel launch shapes (cluster x packs per thread) on the
+    decode and mid-size shapes; graph method, hot and cold; one JSON line
+    per (shape, m).  Feeds the launch plan."""
+    import torch
+    import allreduce_sum_residual_gb300 as arn
+    import synth
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", L2_BYTES_FALLBACK) or L2_BYTES_FALLBACK
+    cases = [(synth.DECODE, m) for m in synth.DECODE.ms] + [(synth.TWO_STAGE, m) for m in (32, 64, 128, 256)]
+    for w, m in cases:
+        base = synth.make_inputs(w, m, backend="torch", device="cuda")
+        set_bytes = algo_bytes(w.n, m, w.H)
+        nsets = max(2, min(64, -(-4 * l2 // set_bytes)))
+        cold = [base] + [synth.make_inputs(w, m, backend="torch", device="cuda", seed=s + 1)
+                         for s in range(nsets - 1)]
+        auto = arn.ar_get_plan(w.n, m, w.H, 1)
+        P = w.H // 8
+        for cluster in (1, 2, 4, 8, 16):
+            for vpt in (1, 2, 4):
+                if -(-P // cluster) > 1024 or -(-(-(-P // cluster)) // vpt) > 1024 // vpt:
+                    continue
+                shape = ("register", cluster, vpt)
+                hot = graph_latency(arn, [base], "one_stage", w.eps, stream, 2000, 20, shape)
+                cold_t = graph_latency(arn, cold, "one_stage", w.eps, stream, 2000, 20, shape)
+                print(json.dumps({"n": w.n, "H": w.H, "m": m, "cluster": cluster, "vpt": vpt,
+                                  "auto": auto["cluster"] == cluster and auto["vpt"] == vpt
+                                  and auto["kernel"] == 1,
+                                  "us_hot": round(hot * 1e6, 3), "us_cold": round(cold_t * 1e6, 3)}),
+                      flush=True)
+        del cold, base
+        torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -570,6 +615,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default="prefill", choices=("prefill", "decode", "two_stage", "tiny"))
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--shapes", action="store_true", help="register-kernel launch-shape sweep")
     ap.add_argument("--quick", action="store_true", help="shorter latency table and baselines")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
@@ -587,6 +633,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.shapes:
+        return run_shapes(args)
     return run_ours(args)
 
 
