@@ -277,6 +277,26 @@ def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=No
     return best / calls
 
 
+def cold_sets(synth, w, m, base, l2_bytes, calls, cap_bytes=8 << 30):
+    """Input sets for a cold-cache graph: views into one pool of bf16 data,
+    one set per call up to `calls`, so that the calls of one replay touch
+    at least ~2.5x the L2 (or every set is already larger than L2).  The
+    weight is shared (it is one H-vector).  Values follow the workload's
+    distributions (drawn once for the pool)."""
+    import torch
+    per_set = (w.n + 1) * m * w.H
+    set_bytes = per_set * 2
+    want = max(2, -(-int(2.5 * l2_bytes) // set_bytes))
+    nsets = int(min(calls, want, max(2, cap_bytes // set_bytes)))
+    pool = synth.normal_bf16((nsets, w.n + 1, m, w.H), 0.0, w.p_std, w.seed, 7,
+                             backend="torch", device="cuda")
+    sets = []
+    for i in range(nsets):
+        parts = [pool[i, k] for k in range(w.n)]
+        sets.append(synth.Inputs(parts, pool[i, w.n], base.weight, base.eps))
+    return sets
+
+
 def latency_table(arn, synth, stream, l2_bytes, quick):
     import torch
     rows = []
@@ -284,15 +304,11 @@ def latency_table(arn, synth, stream, l2_bytes, quick):
         for m in w.ms:
             base = synth.make_inputs(w, m, backend="torch", device="cuda")
             set_bytes = algo_bytes(w.n, m, w.H)
-            nsets = max(2, min(256, -(-4 * l2_bytes // set_bytes)))
-            if quick:
-                nsets = min(nsets, 8)
-            cold = [base] + [synth.make_inputs(w, m, backend="torch", device="cuda", seed=s + 1)
-                             for s in range(nsets - 1)]
             calls = 2000 if set_bytes < 64 << 20 else 200
             replays = 80 if set_bytes < 64 << 20 else 10
             if quick:
-                calls, replays = min(calls, 200), min(replays, 10)
+                replays = min(replays, 10)
+            cold = cold_sets(synth, w, m, base, l2_bytes, calls)
             entry = {"workload": w.name, "n": w.n, "H": w.H, "m": m}
             plan = arn.ar_get_plan(w.n, m, w.H, 0)
             entry["auto_path"] = "two_stage" if plan["mode"] == 2 else "one_stage"
@@ -557,17 +573,16 @@ def run_sweep(args):
     for w in synth.SWEEP:
         for m in w.ms:
             set_bytes = algo_bytes(w.n, m, w.H)
-            nsets = max(2, min(64, -(-4 * l2 // set_bytes)))
-            inps = [synth.make_inputs(w, m, backend="torch", device="cuda", seed=s)
-                    for s in range(nsets)]
             calls = 2000 if set_bytes < 32 << 20 else 100
             replays = 40 if set_bytes < 32 << 20 else 5
-            row = {"n": w.n, "H": w.H, "m": m, "bytes": set_bytes}
+            base = synth.make_inputs(w, m, backend="torch", device="cuda")
+            inps = cold_sets(synth, w, m, base, l2, calls)
+            row = {"n": w.n, "H": w.H, "m": m, "bytes": set_bytes, "sets": len(inps)}
             for mode in ("one_stage", "two_stage"):
                 t = graph_latency(arn, inps, mode, w.eps, stream, calls, replays)
                 row[mode] = {"us": round(t * 1e6, 3), "gbs": round(set_bytes / t / 1e9, 1)}
             print(json.dumps(row), flush=True)
-            del inps
+            del inps, base
             torch.cuda.empty_cache()
 
 
@@ -585,10 +600,7 @@ def run_shapes(args):
     cases = [(synth.DECODE, m) for m in synth.DECODE.ms] + [(synth.TWO_STAGE, m) for m in (32, 64, 128, 256)]
     for w, m in cases:
         base = synth.make_inputs(w, m, backend="torch", device="cuda")
-        set_bytes = algo_bytes(w.n, m, w.H)
-        nsets = max(2, min(64, -(-4 * l2 // set_bytes)))
-        cold = [base] + [synth.make_inputs(w, m, backend="torch", device="cuda", seed=s + 1)
-                         for s in range(nsets - 1)]
+        cold = cold_sets(synth, w, m, base, l2, 2000)
         auto = arn.ar_get_plan(w.n, m, w.H, 1)
         P = w.H // 8
         for cluster in (1, 2, 4, 8, 16):
