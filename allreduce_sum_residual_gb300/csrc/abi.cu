@@ -192,27 +192,38 @@ static int select_mode(int n, int64_t m, int64_t H) {
 }
 
 // The stream kernel takes over from this many rows on (rows alone then give
-// every SM several rows to stream through its ring).
+// every SM several rows to stream through its ring), when the epilogue has
+// at least this many inputs: with a single input (stage 2 of two-stage) its
+// tiles are too small to pay for the ring -- measured on GB300 at m = 2048
+// and 8192, the register kernel did stage 2 in 70-75 % of the time.
 static int64_t stream_min_rows(int sms) { return 2 * static_cast<int64_t>(sms); }
+constexpr int kStreamMinInputs = 2;
 
-// Register kernel: launch shape for m rows of P packs.
-//  * cluster S: the fewest CTAs per row that hold a row in registers
-//    (<= 1024 packs per CTA), then doubled while the grid (m * S) does not
-//    yet give every SM a CTA and each CTA keeps >= 32 packs.
-//  * vpt: when rows alone fill the GPU (m >= 2 * SMs), the fewest packs per
-//    thread that keep a CTA at <= 256 threads (several CTAs per SM);
-//    otherwise 1 pack per thread, i.e. the most loads in flight at once
-//    for a short grid.  Either way a CTA stays within 1024 / vpt threads.
+// Register kernel: launch shape for m rows of P packs.  Set from the GB300
+// launch-shape sweep (the bench's shapes mode: decode n = 8 and mid-size
+// n = 4 at H = 7168, every cluster size x packs per thread, hot and cold):
+//  * cluster S: the fewest CTAs per row that hold a row slice in registers
+//    (<= 1024 packs per CTA); below 32 rows, a row is spread over 8 CTAs
+//    (each keeping >= 32 packs) -- 8 beat 16, 4 and 1 at m <= 16 -- while
+//    from 32 rows on one CTA per row was fastest;
+//  * vpt: 1 pack per thread (the most loads in flight per CTA) below 256
+//    rows, 2 from 256 rows on (the measured best at m = 256), and for very
+//    many rows the fewest packs that keep a CTA at <= 256 threads.  Either
+//    way a CTA stays within 1024 / vpt threads.
 static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
                           ar_plan_t *pl) {
   int S = 1;
   while (S < kMaxClusterCtas && (P + S - 1) / S > kMaxPacksPerCta) S *= 2;
-  while (S < kMaxClusterCtas && m * S < sms && (P + 2 * S - 1) / (2 * S) >= 32) S *= 2;
+  if (m < 32)
+    while (S < 8 && (P + 2 * S - 1) / (2 * S) >= 32) S *= 2;
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
-  if (m >= 2 * static_cast<int64_t>(sms))
+  if (m >= 2 * static_cast<int64_t>(sms)) {
     while (vpt < 8 && (per_cta + vpt - 1) / vpt > 256) vpt *= 2;
+  } else if (m >= 256 && per_cta >= 64) {
+    vpt = 2;
+  }
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
@@ -273,7 +284,8 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
   const bool shape_forced = fc != 0 || fv != 0;
   const bool want_stream =
-      fk == AR_KERNEL_STREAM || (fk == AR_KERNEL_AUTO && !shape_forced && m >= stream_min_rows(sms));
+      fk == AR_KERNEL_STREAM || (fk == AR_KERNEL_AUTO && !shape_forced &&
+                                 m >= stream_min_rows(sms) && inputs >= kStreamMinInputs);
   if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin, pl))) {
     if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
     plan_register(m, P, sms, fc, fv, pl);

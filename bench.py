@@ -619,6 +619,38 @@ def run_shapes(args):
         torch.cuda.empty_cache()
 
 
+def run_kernels(args):
+    """Register vs stream kernel for one-stage at many rows, over n and H
+    (graph method, cold sets); one JSON line per case."""
+    import torch
+    import allreduce_sum_residual_gb300 as arn
+    import synth
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    props = torch.cuda.get_device_properties(0)
+    l2 = getattr(props, "L2_cache_size", L2_BYTES_FALLBACK) or L2_BYTES_FALLBACK
+    for n in (1, 2, 3, 4, 8, 16):
+        for H in (4096, 7168):
+            for m in (304, 1024, 4096, 16384):
+                w = synth.Workload("k", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+                set_bytes = algo_bytes(n, m, H)
+                calls = 2000 if set_bytes < 32 << 20 else 100
+                replays = 20 if set_bytes < 32 << 20 else 5
+                base = synth.make_inputs(w, m, backend="torch", device="cuda")
+                inps = cold_sets(synth, w, m, base, l2, calls)
+                row = {"n": n, "H": H, "m": m, "bytes": set_bytes}
+                for shape in (("stream", 0, 0), ("register", 0, 1), ("register", 0, 2),
+                              ("register", 0, 4), ("register", 0, 8)):
+                    try:
+                        t = graph_latency(arn, inps, "one_stage", w.eps, stream, calls, replays, shape)
+                        row[f"{shape[0]}{shape[2] or ''}"] = round(set_bytes / t / 1e9, 1)
+                    except arn.ArError:
+                        pass
+                print(json.dumps(row), flush=True)
+                del inps, base
+                torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -628,6 +660,7 @@ def main(argv=None):
     ap.add_argument("--workload", default="prefill", choices=("prefill", "decode", "two_stage", "tiny"))
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--shapes", action="store_true", help="register-kernel launch-shape sweep")
+    ap.add_argument("--kernels", action="store_true", help="register vs stream kernel sweep")
     ap.add_argument("--quick", action="store_true", help="shorter latency table and baselines")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
@@ -647,6 +680,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.shapes:
         return run_shapes(args)
+    if args.kernels:
+        return run_kernels(args)
     return run_ours(args)
 
 

@@ -161,8 +161,13 @@ def test_plan_covers_every_pack(arlib, n, m, H, mode):
 
 
 def test_plan_spreads_small_batches(arlib):
-    # decode: a single row of H = 7168 spreads over a 16-CTA cluster
-    assert arlib.ar_get_plan(8, 1, 7168, 1, sm_count=152)["cluster"] == 16
+    # decode: a row of H = 7168 spreads over an 8-CTA cluster below 32 rows
+    for m in (1, 4, 16, 31):
+        assert arlib.ar_get_plan(8, m, 7168, 1, sm_count=152)["cluster"] == 8
+    assert arlib.ar_get_plan(4, 32, 7168, 1, sm_count=152)["cluster"] == 1
+    assert arlib.ar_get_plan(4, 256, 7168, 1, sm_count=152)["vpt"] == 2
+    # stage 2 of two-stage (one input) stays on the register kernel
+    assert arlib.ar_get_plan(8, 8192, 6144, 2, sm_count=152)["kernel"] == 1
     # prefill: rows alone fill the GPU; one persistent streaming CTA per SM
     p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 152
