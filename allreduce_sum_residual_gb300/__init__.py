@@ -181,11 +181,13 @@ def ar_rmsnorm(partials, residual, weight, eps, out=None, residual_out=None,
 
 
 def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
-                  mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0, kernel=0):
+                  mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0, kernel=0,
+                  threads=0, stages=0, ctas=0):
     """ar_rmsnorm plus the reduced sum (fp32 [m, H] ``sum_out``) and a forced
-    kernel ("register" / "stream") and register-kernel launch shape
-    (``cluster`` CTAs per row, ``vpt`` packs per thread); 0 = library's
-    choice.  Returns (out, residual_out, sum_out)."""
+    kernel ("register" / "stream") and launch shape: register kernel
+    ``cluster`` CTAs per row and ``vpt`` packs per thread; stream kernel
+    ``threads`` (32 + consumers), ring ``stages`` and grid ``ctas``.  0 =
+    library's choice.  Returns (out, residual_out, sum_out)."""
     import torch
     mode = MODES.get(mode, mode)
     m, H, dev, out, residual_out, arr = _prepare(partials, residual, weight, out, residual_out)
@@ -195,8 +197,9 @@ def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
             raise ValueError("sum_out must be a contiguous float32 [m, H] tensor on the inputs' device")
     plan = None
     kernel = KERNELS.get(kernel, kernel)
-    if cluster or vpt or kernel:
-        plan = ctypes.pointer(ar_plan_t(0, int(kernel), int(cluster), int(vpt), 0, 0, 0, 0))
+    if cluster or vpt or kernel or threads or stages or ctas:
+        plan = ctypes.pointer(ar_plan_t(0, int(kernel), int(cluster), int(vpt), int(threads),
+                                        int(stages), int(ctas), 0))
     st = lib().ar_rmsnorm_ex(arr, len(partials), _ptr(residual), _ptr(weight), float(eps), m, H,
                              _ptr(out), _ptr(residual_out), int(mode), _stream_ptr(stream, dev),
                              _VP(sum_out.data_ptr()) if sum_out is not None else None, plan)

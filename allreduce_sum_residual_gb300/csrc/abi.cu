@@ -242,15 +242,27 @@ static int64_t stream_smem_bytes(int inputs, int consumers, int stages) {
 
 // Stream kernel: a row is split into V tiles of T_c <= 512 packs (about 256
 // where that gives <= 8 tiles); the ring holds as many slots of (inputs + 1)
-// tiles as fit in shared memory, at most 16.  False if it cannot apply.
-static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_optin, ar_plan_t *pl) {
+// tiles as fit in shared memory, at most 16; one CTA per SM.  A forced plan
+// may set T_c (threads - 32), the ring depth and the grid (several CTAs per
+// SM then share its shared memory).  False if the shape cannot apply.
+static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_optin,
+                        const ar_plan_t *force, ar_plan_t *pl) {
   if (P > AR_STREAM_MAX_HIDDEN / kPackElems) return false;
   int64_t V = (P + 255) / 256;
   if (V > 8) V = (P + kStreamMaxConsumers - 1) / kStreamMaxConsumers;
+  int Tc = static_cast<int>(((P + V - 1) / V + 31) / 32 * 32);
+  if (force && force->threads > 0) {
+    Tc = force->threads - 32;
+    if (Tc < 32 || Tc > kStreamMaxConsumers || Tc % 32 != 0) return false;
+    V = (P + Tc - 1) / Tc;
+  }
   if (V > 8) return false;
-  const int Tc = static_cast<int>(((P + V - 1) / V + 31) / 32 * 32);
-  int stages = 16;
-  while (stages >= 2 && stream_smem_bytes(inputs, Tc, stages) > smem_optin) --stages;
+  int64_t ctas = m < sms ? m : sms;
+  if (force && force->ctas > 0) ctas = force->ctas < m ? force->ctas : m;
+  const int64_t per_sm = (ctas + sms - 1) / sms;
+  const int64_t budget = smem_optin / per_sm - (per_sm > 1 ? 1024 : 0);
+  int stages = force && force->stages > 0 ? force->stages : 16;
+  while (stages >= 2 && stream_smem_bytes(inputs, Tc, stages) > budget) --stages;
   if (stages < 2) return false;
   int vpt = 1;
   while (vpt < V) vpt *= 2;
@@ -259,7 +271,7 @@ static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_opti
   pl->vpt = vpt;
   pl->threads = 32 + Tc;
   pl->stages = stages;
-  pl->ctas = m < sms ? m : sms;
+  pl->ctas = ctas;
   return true;
 }
 
@@ -279,6 +291,10 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
     if (fc != 0 && fc != 1 && fc != 2 && fc != 4 && fc != 8 && fc != 16) return AR_ERR_ARG;
     if (fv != 0 && vpt_log2(fv) < 0) return AR_ERR_ARG;
     if (fk == AR_KERNEL_STREAM && (fc > 1 || fv != 0)) return AR_ERR_ARG;
+    if (fk != AR_KERNEL_STREAM && (force->threads != 0 || force->stages != 0 || force->ctas != 0))
+      return AR_ERR_ARG;
+    if (force->threads < 0 || force->stages < 0 || force->stages > 16 || force->ctas < 0)
+      return AR_ERR_ARG;
   }
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
@@ -286,7 +302,8 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   const bool want_stream =
       fk == AR_KERNEL_STREAM || (fk == AR_KERNEL_AUTO && !shape_forced &&
                                  m >= stream_min_rows(sms) && inputs >= kStreamMinInputs);
-  if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin, pl))) {
+  if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin,
+                                   fk == AR_KERNEL_STREAM ? force : nullptr, pl))) {
     if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
     plan_register(m, P, sms, fc, fv, pl);
     const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;

@@ -241,7 +241,8 @@ def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=
 def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=None):
     """The pages' method: `calls` calls in one CUDA graph (cycling over the
     input sets in `inps`), per-call time = min over replays / calls.
-    `shape` = (kernel, cluster, vpt) forces a launch shape."""
+    `shape` = (kernel, cluster, vpt[, threads, stages, ctas]) forces a
+    launch shape."""
     import torch
     outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
 
@@ -249,8 +250,9 @@ def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=No
         if shape is None:
             arn.ar_rmsnorm(i.partials, i.residual, i.weight, eps, out=o, residual_out=r, mode=mode)
         else:
+            extra = dict(zip(("threads", "stages", "ctas"), shape[3:]))
             arn.ar_rmsnorm_ex(i.partials, i.residual, i.weight, eps, out=o, residual_out=r,
-                              mode=mode, kernel=shape[0], cluster=shape[1], vpt=shape[2])
+                              mode=mode, kernel=shape[0], cluster=shape[1], vpt=shape[2], **extra)
 
     with torch.cuda.stream(stream):
         for i, (o, r) in zip(inps, outs):
@@ -651,6 +653,36 @@ def run_kernels(args):
                 torch.cuda.empty_cache()
 
 
+def run_stream_shapes(args):
+    """Stream-kernel shapes (tile width, CTAs per SM) against the register
+    kernel, one-stage, m = 8192, cold; one JSON line per (n, H)."""
+    import torch
+    import allreduce_sum_residual_gb300 as arn
+    import synth
+    torch.cuda.set_device(0)
+    stream = torch.cuda.Stream()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    m = 8192
+    for n in (3, 4, 8, 16):
+        for H in (4096, 6144, 7168):
+            w = synth.Workload("s", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+            inp = synth.make_inputs(w, m, backend="torch", device="cuda")
+            B = algo_bytes(n, m, H)
+            row = {"n": n, "H": H, "m": m}
+            shapes = [("register", 0, v) for v in (1, 2, 4)] + [
+                ("stream", 0, 0, 32 + tc, 0, c) for tc in (128, 256, 384, 512) for c in (sms, 2 * sms)]
+            for sh in shapes:
+                key = sh[0] + (f"_v{sh[2]}" if sh[0] == "register" else f"_tc{sh[3] - 32}_g{sh[5]}")
+                try:
+                    t = graph_latency(arn, [inp], "one_stage", w.eps, stream, 100, 10, sh)
+                    row[key] = round(B / t / 1e9, 1)
+                except arn.ArError:
+                    row[key] = None
+            print(json.dumps(row), flush=True)
+            del inp
+            torch.cuda.empty_cache()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -661,6 +693,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--shapes", action="store_true", help="register-kernel launch-shape sweep")
     ap.add_argument("--kernels", action="store_true", help="register vs stream kernel sweep")
+    ap.add_argument("--stream-shapes", action="store_true", help="stream-kernel shape sweep")
     ap.add_argument("--quick", action="store_true", help="shorter latency table and baselines")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
@@ -682,6 +715,8 @@ def main(argv=None):
         return run_shapes(args)
     if args.kernels:
         return run_kernels(args)
+    if args.stream_shapes:
+        return run_stream_shapes(args)
     return run_ours(args)
 
 

@@ -146,13 +146,17 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count,
  *            reduced sum feeding the residual add: the fp32 accumulator for
  *            one-stage, the widened bf16 temporary for two-stage.  NULL to
  *            skip.  Costs 4*m*H extra bytes of writes.
- *   plan     NULL for the library's choice, else its `kernel`, `cluster`
- *            and `vpt` fields force the epilogue kernel and, for the register
- *            kernel, its launch shape (0 = library's choice; cluster in
- *            {1,2,4,8,16}, vpt in {1,2,4,8}, at most 1024 packs per CTA; the
- *            stream kernel needs H <= 32768; else AR_ERR_ARG).  The other
- *            fields are ignored; `mode` still picks the path.  The results
- *            do not depend on the kernel or the launch shape.
+ *   plan     NULL for the library's choice, else it forces the epilogue
+ *            kernel and its launch shape; 0 in a field = library's choice.
+ *            `kernel`: AR_KERNEL_REGISTER or AR_KERNEL_STREAM.  Register
+ *            kernel: `cluster` in {1,2,4,8,16}, `vpt` in {1,2,4,8}, at most
+ *            1024 packs per CTA.  Stream kernel (H <= 32768): `threads` =
+ *            32 + consumer threads (a multiple of 32, consumers <= 512, a row
+ *            in <= 8 tiles), `stages` <= 16 ring slots (fewer if shared
+ *            memory is short), `ctas` = grid size (several CTAs per SM split
+ *            its shared memory).  Other combinations return AR_ERR_ARG;
+ *            `mode` and `launches` are ignored (`mode` argument picks the
+ *            path).  The results do not depend on the kernel or the shape.
  */
 int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
                   const void *weight, float eps, int64_t m, int64_t H,
