@@ -193,11 +193,12 @@ static int select_mode(int n, int64_t m, int64_t H) {
 
 // The stream kernel takes over from this many rows on (rows alone then give
 // every SM several rows to stream through its ring), when the epilogue has
-// at least this many inputs: with a single input (stage 2 of two-stage) its
-// tiles are too small to pay for the ring -- measured on GB300 at m = 2048
-// and 8192, the register kernel did stage 2 in 70-75 % of the time.
+// at least this many inputs.  With 1-3 inputs the register kernel with one
+// pack per thread was faster on GB300 at every size measured (up to 7.2
+// TB/s at n = 3), and with one input (stage 2 of two-stage) the ring's
+// tiles are too small to pay for it.
 static int64_t stream_min_rows(int sms) { return 2 * static_cast<int64_t>(sms); }
-constexpr int kStreamMinInputs = 2;
+constexpr int kStreamMinInputs = 4;
 
 // Register kernel: launch shape for m rows of P packs.  Set from the GB300
 // launch-shape sweep (the bench's shapes mode: decode n = 8 and mid-size
@@ -207,9 +208,9 @@ constexpr int kStreamMinInputs = 2;
 //    (each keeping >= 32 packs) -- 8 beat 16, 4 and 1 at m <= 16 -- while
 //    from 32 rows on one CTA per row was fastest;
 //  * vpt: 1 pack per thread (the most loads in flight per CTA) below 256
-//    rows, 2 from 256 rows on (the measured best at m = 256), and for very
-//    many rows the fewest packs that keep a CTA at <= 256 threads.  Either
-//    way a CTA stays within 1024 / vpt threads.
+//    rows, 2 from 256 rows on (the measured best at m = 256, and within a
+//    few per cent of the best for 1-3 inputs at m up to 16384).  Either way
+//    a CTA stays within 1024 / vpt threads.
 static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
                           ar_plan_t *pl) {
   int S = 1;
@@ -219,11 +220,7 @@ static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int 
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
-  if (m >= 2 * static_cast<int64_t>(sms)) {
-    while (vpt < 8 && (per_cta + vpt - 1) / vpt > 256) vpt *= 2;
-  } else if (m >= 256 && per_cta >= 64) {
-    vpt = 2;
-  }
+  if (m >= 256 && per_cta >= 64) vpt = 2;
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
@@ -240,11 +237,18 @@ static int64_t stream_smem_bytes(int inputs, int consumers, int stages) {
   return static_cast<int64_t>(stages) * (inputs + 1) * consumers * 16 + 16 * stages + 64 * 4 + 16;
 }
 
-// Stream kernel: a row is split into V tiles of T_c <= 512 packs (about 256
-// where that gives <= 8 tiles); the ring holds as many slots of (inputs + 1)
-// tiles as fit in shared memory, at most 16; one CTA per SM.  A forced plan
-// may set T_c (threads - 32), the ring depth and the grid (several CTAs per
-// SM then share its shared memory).  False if the shape cannot apply.
+// Stream kernel.  A row is split into V tiles of T_c <= 512 packs (about
+// 256 where that gives <= 8 tiles).  The ring is sized for about
+// kStreamInflightBytes in flight per SM: 2 CTAs per SM when two rings of
+// 2 slots fit in shared memory, else 1, and as many slots as that target
+// allows (>= 2).  Measured on GB300 (one-stage, m = 8192, n = 4 / 8 / 16,
+// H = 4096 .. 8192, three repeats within 0.1 %): 120-144 KB in flight per
+// SM ran at 7.0-7.2 TB/s, while filling shared memory (216 KB) ran at
+// 6.4 TB/s -- deeper queues of outstanding bulk copies hurt.  A forced plan
+// may set T_c (threads - 32), the ring depth and the grid.  False if the
+// shape cannot apply.
+constexpr int64_t kStreamInflightBytes = 144 * 1024;
+
 static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_optin,
                         const ar_plan_t *force, ar_plan_t *pl) {
   if (P > AR_STREAM_MAX_HIDDEN / kPackElems) return false;
@@ -257,13 +261,24 @@ static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_opti
     V = (P + Tc - 1) / Tc;
   }
   if (V > 8) return false;
-  int64_t ctas = m < sms ? m : sms;
-  if (force && force->ctas > 0) ctas = force->ctas < m ? force->ctas : m;
-  const int64_t per_sm = (ctas + sms - 1) / sms;
+  const int64_t slot = static_cast<int64_t>(inputs + 1) * Tc * 16;
+  // Two CTAs per SM need two 2-slot rings in shared memory and their threads'
+  // registers in the register file (<= 96 registers a thread: T_c <= 288).
+  const int64_t half_budget = smem_optin / 2 - 1024;
+  int64_t per_sm = (stream_smem_bytes(inputs, Tc, 2) <= half_budget && Tc <= 288) ? 2 : 1;
+  int64_t ctas = per_sm * sms;
+  int stages = static_cast<int>(kStreamInflightBytes / (per_sm * slot));
+  if (force && force->ctas > 0) {
+    ctas = force->ctas;
+    per_sm = (ctas + sms - 1) / sms;
+  }
+  if (force && force->stages > 0) stages = force->stages;
+  if (stages > 16) stages = 16;
+  if (stages < 2) stages = 2;
   const int64_t budget = smem_optin / per_sm - (per_sm > 1 ? 1024 : 0);
-  int stages = force && force->stages > 0 ? force->stages : 16;
   while (stages >= 2 && stream_smem_bytes(inputs, Tc, stages) > budget) --stages;
   if (stages < 2) return false;
+  if (ctas > m) ctas = m;
   int vpt = 1;
   while (vpt < V) vpt *= 2;
   pl->kernel = AR_KERNEL_STREAM;

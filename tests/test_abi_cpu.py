@@ -156,8 +156,9 @@ def test_plan_covers_every_pack(arlib, n, m, H, mode):
         assert tiles <= p["vpt"]                           # the template holds every tile
         inputs = n if p["mode"] == 1 else 1
         smem = p["stages"] * (inputs + 1) * tc * 16 + 16 * p["stages"] + 256 + 16
-        assert 2 <= p["stages"] <= 16 and smem <= 232448
-        assert p["ctas"] == min(m, 152)
+        per_sm = -(-p["ctas"] // 152)
+        assert 2 <= p["stages"] <= 16 and per_sm * (smem + 1024) <= 233472
+        assert p["ctas"] in (min(m, 152), min(m, 304))
 
 
 def test_plan_spreads_small_batches(arlib):
@@ -168,9 +169,15 @@ def test_plan_spreads_small_batches(arlib):
     assert arlib.ar_get_plan(4, 256, 7168, 1, sm_count=152)["vpt"] == 2
     # stage 2 of two-stage (one input) stays on the register kernel
     assert arlib.ar_get_plan(8, 8192, 6144, 2, sm_count=152)["kernel"] == 1
-    # prefill: rows alone fill the GPU; one persistent streaming CTA per SM
+    # prefill: rows alone fill the GPU; two persistent streaming CTAs per SM,
+    # each with a 2-slot ring of 9 x 4 KB tiles (144 KB in flight per SM)
     p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
-    assert p["kernel"] == 2 and p["ctas"] == 152
+    assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 2 and p["threads"] == 288
+    # 16 inputs: one CTA per SM, 2 slots of 17 x 4 KB
+    p = arlib.ar_get_plan(16, 8192, 6144, 1, sm_count=152)
+    assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2
+    # 3 inputs: the register kernel
+    assert arlib.ar_get_plan(3, 8192, 4096, 1, sm_count=152)["kernel"] == 1
     # H above the stream kernel's limit: the register kernel with a cluster
     p = arlib.ar_get_plan(3, 1000, 65536, 1, sm_count=152)
     assert p["kernel"] == 1 and p["cluster"] == 8
