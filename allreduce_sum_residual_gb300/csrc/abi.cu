@@ -191,13 +191,18 @@ static int select_mode(int n, int64_t m, int64_t H) {
   return m <= one_stage_max_rows(n, H) ? AR_MODE_ONE_STAGE : AR_MODE_TWO_STAGE;
 }
 
-// The stream kernel takes over from this many rows on (rows alone then give
-// every SM several rows to stream through its ring), when the epilogue has
-// at least this many inputs.  With 1-3 inputs the register kernel with one
-// pack per thread was faster on GB300 at every size measured (up to 7.2
-// TB/s at n = 3), and with one input (stage 2 of two-stage) the ring's
-// tiles are too small to pay for it.
-static int64_t stream_min_rows(int sms) { return 2 * static_cast<int64_t>(sms); }
+// The stream kernel takes over from this many rows on, when the epilogue
+// has at least kStreamMinInputs inputs.  Measured on GB300 (the bench's
+// kernels mode, one-stage, cold, n in {1, 2, 3, 4, 8, 16}, H in {4096,
+// 7168}, m in {304, 1024, 4096, 16384}): from 1024 rows on the stream
+// kernel was fastest for n = 8 (up to 7.18 TB/s) and n = 16 (at H = 4096),
+// at 304 rows the register kernel with 2 packs per thread won; with 1-3
+// inputs the register kernel with one pack per thread won at every size (up
+// to 7.19 TB/s at n = 3), and with one input (stage 2 of two-stage) the
+// ring's tiles are too small to pay for it.
+static int64_t stream_min_rows(int sms) {
+  return 4 * static_cast<int64_t>(sms) > 1024 ? 4 * static_cast<int64_t>(sms) : 1024;
+}
 constexpr int kStreamMinInputs = 4;
 
 // Register kernel: launch shape for m rows of P packs.  Set from the GB300
