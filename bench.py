@@ -299,6 +299,70 @@ def cold_sets(synth, w, m, base, l2_bytes, calls, cap_bytes=8 << 30):
     return sets
 
 
+def unfused_torch_us(inp, stream, calls=50, replays=5):
+    """Comparator only (never the product path): the same epilogue as
+    separate torch ops -- rank-order fp32 sum, bf16 round (what an
+    all-reduce returns), residual add, torch RMSNorm -- in one CUDA graph;
+    per-call time = fastest replay / calls."""
+    import torch
+    H = inp.residual.shape[1]
+    w = inp.weight.float()
+
+    def call():
+        s = inp.partials[0].float()
+        for p in inp.partials[1:]:
+            s = s + p.float()
+        r = s.to(torch.bfloat16).float() + inp.residual.float()
+        rout = r.to(torch.bfloat16)
+        out = torch.nn.functional.rms_norm(r, (H,), w, eps=inp.eps).to(torch.bfloat16)
+        return out, rout
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            call()
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+    del g
+    return best / calls * 1e6
+
+
+def empty_node_floor_us(stream, calls=2000, replays=20):
+    """Per-node time of a graph of back-to-back trivial kernels (a one-element
+    fill): the launch-and-complete floor any dependent kernel chain pays."""
+    import torch
+    x = torch.zeros(1, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            x.fill_(1.0)
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+    del g
+    return best / calls * 1e6
+
+
 def latency_table(arn, synth, stream, l2_bytes, quick):
     import torch
     rows = []
@@ -470,6 +534,11 @@ def run_ours(args):
         if not args.kernel_only:
             if not args.no_latency:
                 lat = latency_table(arn, synth, stream, l2, args.quick)
+                modes["unfused_torch"] = {"us": round(unfused_torch_us(inp, stream), 2),
+                                          "note": "comparator: separate torch ops in a graph"}
+                modes["unfused_torch"]["gbs"] = round(bytes_step / modes["unfused_torch"]["us"]
+                                                      / 1e3, 1)
+                floor = empty_node_floor_us(stream)
             e2e_t, h2d, d2h = e2e_measure(arn, inp, step_mode, stream, 3 if args.quick else 10)
             e2e = {"value": round(bytes_step / e2e_t / 1e9, 2), "unit": "GB/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -501,6 +570,7 @@ def run_ours(args):
             "gpu_launches": args.steps * plan["launches"],
             "clocks": clocks,
             "latency_vs_m": lat,
+            "empty_kernel_node_floor_us": round(floor, 3) if lat else None,
         }
         print(json.dumps(result), flush=True)
     if world > 1:
