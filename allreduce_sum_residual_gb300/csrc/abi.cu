@@ -244,15 +244,18 @@ static int64_t stream_smem_bytes(int inputs, int consumers, int stages) {
 
 // Stream kernel.  A row is split into V tiles of T_c <= 512 packs (about
 // 256 where that gives <= 8 tiles).  The ring is sized for about
-// kStreamInflightBytes in flight per SM: 2 CTAs per SM when two rings of
-// 2 slots fit in shared memory, else 1, and as many slots as that target
-// allows (>= 2).  Measured on GB300 (one-stage, m = 8192, n = 4 / 8 / 16,
-// H = 4096 .. 8192, three repeats within 0.1 %): 120-144 KB in flight per
-// SM ran at 7.0-7.2 TB/s, while filling shared memory (216 KB) ran at
-// 6.4 TB/s -- deeper queues of outstanding bulk copies hurt.  A forced plan
-// may set T_c (threads - 32), the ring depth and the grid.  False if the
-// shape cannot apply.
-constexpr int64_t kStreamInflightBytes = 144 * 1024;
+// kStreamInflightBytes of bulk copies in flight per SM: 2 CTAs per SM while
+// two 2-slot rings stay within kStreamTwoCtaMaxBytes (and fit in shared
+// memory and the register file), else 1, each with as many slots as the
+// target allows (>= 2).  Measured on GB300 (one-stage, m = 8192, n = 4 ..
+// 16, H = 4096 .. 8192, repeats within 0.1-0.5 %): about 100-150 KB in
+// flight per SM ran at 7.0-7.2 TB/s, filling shared memory (216 KB) at
+// 6.3-6.4 TB/s -- deeper queues of outstanding bulk copies are slower; at
+// n = 4 three 18 KB slots per CTA beat four by 7 %, and with >= 12 inputs
+// one CTA per SM beat two.  A forced plan may set T_c (threads - 32), the
+// ring depth and the grid.  False if the shape cannot apply.
+constexpr int64_t kStreamInflightBytes = 120 * 1024;
+constexpr int64_t kStreamTwoCtaMaxBytes = 160 * 1024;
 
 static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_optin,
                         const ar_plan_t *force, ar_plan_t *pl) {
@@ -270,7 +273,10 @@ static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_opti
   // Two CTAs per SM need two 2-slot rings in shared memory and their threads'
   // registers in the register file (<= 96 registers a thread: T_c <= 288).
   const int64_t half_budget = smem_optin / 2 - 1024;
-  int64_t per_sm = (stream_smem_bytes(inputs, Tc, 2) <= half_budget && Tc <= 288) ? 2 : 1;
+  int64_t per_sm = (stream_smem_bytes(inputs, Tc, 2) <= half_budget && Tc <= 288 &&
+                    4 * slot <= kStreamTwoCtaMaxBytes)
+                       ? 2
+                       : 1;
   int64_t ctas = per_sm * sms;
   int stages = static_cast<int>(kStreamInflightBytes / (per_sm * slot));
   if (force && force->ctas > 0) {

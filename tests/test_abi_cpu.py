@@ -173,9 +173,13 @@ def test_plan_spreads_small_batches(arlib):
     # each with a 2-slot ring of 9 x 4 KB tiles (144 KB in flight per SM)
     p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 2 and p["threads"] == 288
-    # 16 inputs: one CTA per SM, 2 slots of 17 x 4 KB
-    p = arlib.ar_get_plan(16, 8192, 6144, 1, sm_count=152)
-    assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2
+    # 4 inputs, H = 7168: two CTAs per SM with 3 slots of 5 x 3.5 KB
+    p = arlib.ar_get_plan(4, 8192, 7168, 1, sm_count=152)
+    assert p["ctas"] == 304 and p["stages"] == 3 and p["threads"] == 32 + 224
+    # 12 and 16 inputs: one CTA per SM, 2 slots
+    for n in (12, 16):
+        p = arlib.ar_get_plan(n, 8192, 6144, 1, sm_count=152)
+        assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2
     # 3 inputs: the register kernel
     assert arlib.ar_get_plan(3, 8192, 4096, 1, sm_count=152)["kernel"] == 1
     # H above the stream kernel's limit: the register kernel with a cluster
