@@ -12,6 +12,7 @@ Names follow the C ABI:
                mode=AR_MODE_AUTO, stream=None) -> (out, residual_out)
     ar_rmsnorm_ex(..., sum_out=None, cluster=0, vpt=0)
     ar_reduce_scatter_flat(partials, temp, stream=None)
+    ar_reduce_scatter_store(partials, temps, rank, stream=None)
     ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None)
     ar_reserve_workspace(max_elems, device) / ar_release_workspace(device)
     ar_workspace_elems(device), ar_select_mode(n, m, H),
@@ -74,6 +75,8 @@ _SIGS = {
     "ar_get_plan": (ctypes.c_int, [ctypes.c_int, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(ar_plan_t)]),
     "ar_reduce_scatter_flat": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _I64, _VP, _VP]),
+    "ar_reduce_scatter_store": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _I64, ctypes.c_int,
+                                               ctypes.c_int, ctypes.POINTER(_VP), _VP]),
     "ar_load_rmsnorm": (ctypes.c_int, [_VP, _VP, _VP, ctypes.c_float, _I64, _I64, _VP, _VP, _VP]),
     "ar_reserve_workspace": (ctypes.c_int, [_I64, ctypes.c_int]),
     "ar_release_workspace": (ctypes.c_int, [ctypes.c_int]),
@@ -232,6 +235,23 @@ def ar_reduce_scatter_flat(partials, temp, stream=None):
                                       _stream_ptr(stream, temp.device))
     _check(st, "ar_reduce_scatter_flat")
     return temp
+
+
+def ar_reduce_scatter_store(partials, temps, rank, stream=None):
+    """Stage 1 as rank `rank` of len(temps) ranks: reduce this rank's slice
+    of the packs and store bf16(sum) into every buffer of `temps`."""
+    shape = tuple(temps[0].shape)
+    dev = temps[0].device
+    for k, p in enumerate(partials):
+        _check_tensor(p, f"partials[{k}]", shape, dev)
+    for d, t in enumerate(temps):
+        _check_tensor(t, f"temps[{d}]", shape, dev)
+    arr = (_VP * len(partials))(*[p.data_ptr() for p in partials])
+    tarr = (_VP * len(temps))(*[t.data_ptr() for t in temps])
+    st = lib().ar_reduce_scatter_store(arr, len(partials), temps[0].numel(), int(rank), len(temps),
+                                       tarr, _stream_ptr(stream, dev))
+    _check(st, "ar_reduce_scatter_store")
+    return temps
 
 
 def ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None, stream=None):

@@ -477,8 +477,10 @@ static int run(const void *const *partials, int n, const void *residual, const v
   ReduceArgs ra;
   std::memset(&ra, 0, sizeof ra);
   for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
-  ra.temp = static_cast<uint4 *>(ws);
-  ra.npacks = m * H / kPackElems;
+  ra.dst[0] = static_cast<uint4 *>(ws);
+  ra.ndst = 1;
+  ra.begin = 0;
+  ra.end = m * H / kPackElems;
   if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   const void *temp_in[1] = {ws};
   return epilogue(temp_in, 1, true);
@@ -512,8 +514,10 @@ int two_stage_with_temp(const void *const *partials, int n, const void *residual
   ReduceArgs ra;
   std::memset(&ra, 0, sizeof ra);
   for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
-  ra.temp = static_cast<uint4 *>(temp);
-  ra.npacks = m * H / kPackElems;
+  ra.dst[0] = static_cast<uint4 *>(temp);
+  ra.ndst = 1;
+  ra.begin = 0;
+  ra.end = m * H / kPackElems;
   if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   const void *temp_in[1] = {temp};
   cudaError_t e;
@@ -628,8 +632,55 @@ int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count, vo
   ReduceArgs ra;
   std::memset(&ra, 0, sizeof ra);
   for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
-  ra.temp = static_cast<uint4 *>(temp);
-  ra.npacks = count / kPackElems;
+  ra.dst[0] = static_cast<uint4 *>(temp);
+  ra.ndst = 1;
+  ra.begin = 0;
+  ra.end = count / kPackElems;
+  return launch_reduce_flat(ra, n, d->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? AR_OK
+             : AR_ERR_CUDA;
+}
+
+int ar_reduce_scatter_store(const void *const *partials, int n, int64_t count, int rank,
+                            int world, void *const *temps, void *stream) {
+  if (n < 1 || n > AR_MAX_RANKS || count < 0 || world < 1 || world > AR_MAX_RANKS || rank < 0 ||
+      rank >= world)
+    return AR_ERR_ARG;
+  if (count % kPackElems != 0) return AR_ERR_ALIGN;
+  if (count > (int64_t{1} << 40)) return AR_ERR_UNSUPPORTED;
+  if (count == 0) return AR_OK;  // nothing is read or written; pointers may be null
+  if (!partials || !temps) return AR_ERR_ARG;
+  for (int k = 0; k < n; ++k)
+    if (!partials[k]) return AR_ERR_ARG;
+  for (int d = 0; d < world; ++d)
+    if (!temps[d]) return AR_ERR_ARG;
+  for (int k = 0; k < n; ++k)
+    if (!aligned16(partials[k])) return AR_ERR_ALIGN;
+  for (int d = 0; d < world; ++d)
+    if (!aligned16(temps[d])) return AR_ERR_ALIGN;
+  const int64_t bytes = count * 2;
+  for (int d = 0; d < world; ++d) {
+    const Range t = range_of(temps[d], bytes);
+    for (int k = 0; k < n; ++k)
+      if (overlap(t, range_of(partials[k], bytes))) return AR_ERR_ALIAS;
+    for (int e = d + 1; e < world; ++e)
+      if (overlap(t, range_of(temps[e], bytes))) return AR_ERR_ALIAS;
+  }
+  const int64_t npacks = count / kPackElems;
+  const int64_t per = (npacks + world - 1) / world;
+  const int64_t begin = static_cast<int64_t>(rank) * per;
+  const int64_t end = begin + per < npacks ? begin + per : npacks;
+  if (begin >= end) return AR_OK;  // this rank's slice is empty
+  int st;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  ReduceArgs ra;
+  std::memset(&ra, 0, sizeof ra);
+  for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
+  for (int e = 0; e < world; ++e) ra.dst[e] = static_cast<uint4 *>(temps[e]);
+  ra.ndst = world;
+  ra.begin = begin;
+  ra.end = end;
   return launch_reduce_flat(ra, n, d->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? AR_OK
              : AR_ERR_CUDA;

@@ -34,10 +34,15 @@ struct EpilogueArgs {
 };
 
 // Kernel parameters of stage 1 (flat reduce of every pack across ranks).
+// Stage 1 reduces the packs [begin, end) and stores each bf16 sum at the
+// same position of every destination dst[0 .. ndst-1] (ndst = 1 for the
+// two-stage temporary; one per rank for the all-gather by stores).
 struct ReduceArgs {
   const uint4 *p[AR_MAX_RANKS];
-  uint4 *temp;
-  int64_t npacks;
+  uint4 *dst[AR_MAX_RANKS];
+  int ndst;
+  int64_t begin;
+  int64_t end;
 };
 
 // --- bf16 <-> fp32 ----------------------------------------------------------

@@ -7,10 +7,14 @@
 // to bf16 and stores it; no shared memory and no block barrier; the rank
 // order ptrs[0..n-1] is kept.  Stage-1 launch config: 256-thread blocks.
 //
-// On one GPU the "scatter" has one destination (this GPU's temporary).  The
-// grid is a multiple of the SM count and strides over all packs; each step
-// of a thread handles U packs 256 apart, issuing all U*n loads before the
-// first add.
+// A launch covers the pack range [begin, end) and stores every sum into
+// ndst destinations at the same position.  The two-stage path uses the
+// whole range and one destination (this GPU's temporary).  One rank of a
+// reduce-scatter uses its slice and one destination per rank -- the page's
+// "writes it to every rank's temporary buffer directly"; across GPUs those
+// would be peer-mapped buffers.  The grid is a multiple of the SM count and
+// strides over the range; each step of a thread handles U packs 256 apart,
+// issuing all U*n loads before the first add.
 #include "epilogue.cuh"
 
 namespace arn {
@@ -25,18 +29,21 @@ k_reduce_flat(const __grid_constant__ ReduceArgs a) {
   pdl_wait_prior_grid();
   pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads * U;
-  for (int64_t i0 = static_cast<int64_t>(blockIdx.x) * kReduceThreads * U + threadIdx.x;
-       i0 < a.npacks; i0 += stride) {
+  for (int64_t i0 = a.begin + static_cast<int64_t>(blockIdx.x) * kReduceThreads * U + threadIdx.x;
+       i0 < a.end; i0 += stride) {
     float acc[U][8];
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t idx = i0 + static_cast<int64_t>(u) * kReduceThreads;
-      if (idx < a.npacks) sum_pack_in_rank_order<N>(a.p, idx, acc[u]);
+      if (idx < a.end) sum_pack_in_rank_order<N>(a.p, idx, acc[u]);
     }
 #pragma unroll
     for (int u = 0; u < U; ++u) {
       const int64_t idx = i0 + static_cast<int64_t>(u) * kReduceThreads;
-      if (idx < a.npacks) st_stream(a.temp + idx, pack8(acc[u]));
+      if (idx < a.end) {
+        const uint4 v = pack8(acc[u]);
+        for (int d = 0; d < a.ndst; ++d) st_stream(a.dst[d] + idx, v);
+      }
     }
   }
 }
@@ -54,10 +61,10 @@ static ReduceKernel reduce_kernel(int n) {
   return table[n - 1];
 }
 
-// Launch stage 1 over `npacks` packs; `sms` is the device's SM count.
+// Launch stage 1 over the pack range of `a`; `sms` is the device's SM count.
 cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream) {
   const int64_t per_block = static_cast<int64_t>(kReduceThreads) * kReduceUnroll;
-  int64_t blocks = (a.npacks + per_block - 1) / per_block;
+  int64_t blocks = (a.end - a.begin + per_block - 1) / per_block;
   const int64_t cap = static_cast<int64_t>(sms) * (2048 / kReduceThreads);
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;

@@ -339,6 +339,45 @@ def unfused_torch_us(inp, stream, calls=50, replays=5):
     return best / calls * 1e6
 
 
+def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
+    """Two-stage with the gather done by stores, all ranks on this GPU: for
+    rank r = 0 .. n-1, ar_reduce_scatter_store reduces slice r and writes it
+    into n temporaries (one per rank), then stage 2 runs on temps[0].  The
+    n-copy write is what a real reduce-scatter + all-gather costs in stores
+    (here to local memory).  Per-call time = fastest replay / calls."""
+    import torch
+    n = len(inp.partials)
+    temps = [torch.empty_like(inp.residual) for _ in range(n)]
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+
+    def call():
+        for r in range(n):
+            arn.ar_reduce_scatter_store(inp.partials, temps, r)
+        arn.ar_load_rmsnorm(temps[0], inp.residual, inp.weight, inp.eps, out=out, residual_out=rout)
+
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            call()
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+    del g, temps
+    return best / calls * 1e6
+
+
 def empty_node_floor_us(stream, calls=2000, replays=20):
     """Per-node time of a graph of back-to-back trivial kernels (a one-element
     fill): the launch-and-complete floor any dependent kernel chain pays."""
@@ -539,6 +578,12 @@ def run_ours(args):
                 modes["unfused_torch"]["gbs"] = round(bytes_step / modes["unfused_torch"]["us"]
                                                       / 1e3, 1)
                 floor = empty_node_floor_us(stream)
+                t_ag = allgather_two_stage_us(arn, inp, stream)
+                ag_bytes = bytes_step + (n + 1) * m * H * 2  # n temp copies written + one read back
+                modes["two_stage_allgather_stores"] = {
+                    "us": round(t_ag, 2), "gbs": round(bytes_step / t_ag / 1e3, 1),
+                    "gbs_actual_bytes": round(ag_bytes / t_ag / 1e3, 1),
+                    "note": "n rank slices each stored into n temporaries, then stage 2"}
             e2e_t, h2d, d2h = e2e_measure(arn, inp, step_mode, stream, 3 if args.quick else 10)
             e2e = {"value": round(bytes_step / e2e_t / 1e9, 2), "unit": "GB/s",
                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -174,6 +174,29 @@ int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count,
                            void *temp, void *stream);
 
 /*
+ * Stage 1 as one rank of `world` runs it in a reduce-scatter whose gather
+ * is done by stores: the packs of slice `rank` -- pack range [rank*S,
+ * min((rank+1)*S, count/8)) with S = ceil(count/8 / world) -- are reduced
+ * across the n partials (fp32, rank order) and bf16(sum) is stored at the
+ * same positions of every buffer temps[0 .. world-1] (ROCm/aiter #3817,
+ * Technical Details, 2stage, reduce-scatter: each pack is reduced and
+ * written "to every rank's temporary buffer directly").  Once all `world`
+ * ranks have run it, and synchronised, every temp holds the whole bf16 sum
+ * and stage 2 (ar_load_rmsnorm) can run on any of them.
+ *   partials  host array of n device pointers, count bf16 each.
+ *   temps     host array of `world` device pointers, count bf16 each; on
+ *             one GPU local buffers (the n-copy write of the all-gather is
+ *             then measured), across GPUs peer-mapped ones (the caller
+ *             provides them and the barrier between the stages).
+ *   world     1 .. AR_MAX_RANKS; rank in [0, world).
+ * count must be a multiple of 8; no temp may overlap a partial or another
+ * temp (AR_ERR_ALIAS); a rank whose slice is empty launches nothing.
+ */
+int ar_reduce_scatter_store(const void *const *partials, int n, int64_t count,
+                            int rank, int world, void *const *temps,
+                            void *stream);
+
+/*
  * Stage 2 alone: the epilogue with a single, already reduced input `temp`
  * ([m, H] bf16): r = temp + residual, then RMSNorm (ROCm/aiter #3817,
  * Technical Details, 2stage, stage-2 RMSNorm reduce:

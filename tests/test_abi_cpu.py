@@ -192,3 +192,25 @@ def test_plan_rejects_bad_shapes(arlib):
         arlib.ar_get_plan(8, 4, 1020, 1, sm_count=152)
     with pytest.raises(arlib.ArError):
         arlib.ar_get_plan(8, 4, 1024, 7, sm_count=152)
+
+
+def test_reduce_scatter_store_checks_arguments(arlib):
+    L = arlib.lib()
+    P = (ctypes.c_void_p * 2)(BASE, BASE + (1 << 20))
+    T = (ctypes.c_void_p * 4)(BASE + (4 << 20), BASE + (5 << 20), BASE + (6 << 20), BASE + (7 << 20))
+    call = L.ar_reduce_scatter_store
+    assert call(P, 2, 1024, 0, 0, T, None) == ARG          # world 0
+    assert call(P, 2, 1024, 4, 4, T, None) == ARG          # rank == world
+    assert call(P, 2, 1024, -1, 4, T, None) == ARG
+    assert call(P, 2, 1024, 0, 17, T, None) == ARG
+    assert call(P, 2, 1020, 0, 4, T, None) == ALIGN        # count % 8
+    assert call(P, 2, 0, 0, 4, None, None) == OK           # empty call needs no pointers
+    Tover = (ctypes.c_void_p * 2)(BASE + (4 << 20), BASE + (4 << 20) + 512)
+    assert call(P, 2, 1024, 0, 2, Tover, None) == ALIAS    # temps overlap each other
+    Tpart = (ctypes.c_void_p * 2)(BASE + 64, BASE + (5 << 20))
+    assert call(P, 2, 1024, 0, 2, Tpart, None) == ALIAS    # a temp overlaps a partial
+    Tmis = (ctypes.c_void_p * 2)(BASE + (4 << 20) + 8, BASE + (5 << 20))
+    assert call(P, 2, 1024, 0, 2, Tmis, None) == ALIGN
+    # one pack spread over 4 ranks: ranks 1..3 have empty slices and launch nothing
+    for r in (1, 2, 3):
+        assert call(P, 2, 8, r, 4, T, None) == OK

@@ -280,6 +280,47 @@ def test_stage_entry_points():
     compare((out, rout, None), (o_out, o_rout, o_sum), "stage 2")
 
 
+@pytest.mark.parametrize("world", [1, 2, 3, 4, 8, 16])
+def test_reduce_scatter_store_every_rank_fills_every_temp(world):
+    """All `world` ranks of the reduce-scatter with gather-by-stores: each
+    temp ends up holding the whole bf16 sum bit-exactly, and stage 2 on any
+    of them gives the two-stage result."""
+    w = synth.Workload("rs", n=4, H=1032, ms=(7,), p_std=0.5, res_std=1.0, seed=world)
+    inp = device_inputs(w, 7)
+    m, H = inp.residual.shape
+    temps = [torch.full((m, H), 0x5A5A, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+             for _ in range(world)]
+    for r in range(world):
+        arn.ar_reduce_scatter_store(inp.partials, temps, r)
+    torch.cuda.synchronize()
+    o_out, o_rout, o_sum = oracle_rows(inp, None, two_stage=True)
+    for t in temps:
+        assert np.array_equal(to_f32(synth.bits(t)).view(np.uint32), o_sum.view(np.uint32))
+    out, rout = arn.ar_load_rmsnorm(temps[-1], inp.residual, inp.weight, w.eps)
+    torch.cuda.synchronize()
+    compare((out, rout, None), (o_out, o_rout, o_sum), f"gathered temp, world={world}")
+
+
+def test_reduce_scatter_store_writes_only_its_slice():
+    w = synth.Workload("rs", n=3, H=4104, ms=(5,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, 5)
+    m, H = inp.residual.shape
+    world, rank = 4, 2
+    temps = [torch.full((m, H), 0x5A5A, dtype=torch.int16, device="cuda").view(torch.bfloat16)
+             for _ in range(world)]
+    arn.ar_reduce_scatter_store(inp.partials, temps, rank)
+    torch.cuda.synchronize()
+    npacks = m * H // 8
+    per = -(-npacks // world)
+    lo, hi = rank * per * 8, min(npacks, (rank + 1) * per) * 8
+    _, _, o_sum = oracle_rows(inp, None, two_stage=True)
+    want = o_sum.ravel()[lo:hi].view(np.uint32)
+    for t in temps:
+        bits = synth.bits(t).ravel()
+        assert np.all(bits[:lo] == 0x5A5A) and np.all(bits[hi:] == 0x5A5A)
+        assert np.array_equal(to_f32(bits[lo:hi]).view(np.uint32), want)
+
+
 # ------------------------------------------------------------------ runtime
 
 def test_graph_capture_and_replay():
