@@ -212,10 +212,13 @@ constexpr int kStreamMinInputs = 4;
 //    (<= 1024 packs per CTA); below 32 rows, a row is spread over 8 CTAs
 //    (each keeping >= 32 packs) -- 8 beat 16, 4 and 1 at m <= 16 -- while
 //    from 32 rows on one CTA per row was fastest;
-//  * vpt: 1 pack per thread (the most loads in flight per CTA) below 256
-//    rows, 2 from 256 rows on (the measured best at m = 256, and within a
-//    few per cent of the best for 1-3 inputs at m up to 16384).  Either way
-//    a CTA stays within 1024 / vpt threads.
+//  * vpt: 1 pack per thread (the most loads in flight per CTA), except 2
+//    for 256 .. 1023 rows of more than 512 packs: a CTA of up to 1024
+//    threads then fits once per SM and the rows would run in two waves;
+//    448-thread CTAs fit twice (measured at H = 7168: m = 256-304 runs
+//    1.1-1.3x faster with 2, while from 1024 rows 1 pack per thread is up
+//    to 1.2x faster for 1-3 inputs).  Either way a CTA stays within
+//    1024 / vpt threads.
 static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
                           ar_plan_t *pl) {
   int S = 1;
@@ -225,7 +228,7 @@ static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int 
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
-  if (m >= 256 && per_cta >= 64) vpt = 2;
+  if (m >= 256 && m < 1024 && per_cta > 512) vpt = 2;
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);

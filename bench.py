@@ -846,11 +846,12 @@ def run_kernels(args):
                 base = synth.make_inputs(w, m, backend="torch", device="cuda")
                 inps = cold_sets(synth, w, m, base, l2, calls)
                 row = {"n": n, "H": H, "m": m, "bytes": set_bytes}
-                for shape in (("stream", 0, 0), ("register", 0, 1), ("register", 0, 2),
+                for shape in (None, ("stream", 0, 0), ("register", 0, 1), ("register", 0, 2),
                               ("register", 0, 4), ("register", 0, 8)):
+                    key = "auto" if shape is None else f"{shape[0]}{shape[2] or ''}"
                     try:
                         t = graph_latency(arn, inps, "one_stage", w.eps, stream, calls, replays, shape)
-                        row[f"{shape[0]}{shape[2] or ''}"] = round(set_bytes / t / 1e9, 1)
+                        row[key] = round(set_bytes / t / 1e9, 1)
                     except arn.ArError:
                         pass
                 print(json.dumps(row), flush=True)
