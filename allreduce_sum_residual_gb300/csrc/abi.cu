@@ -217,10 +217,11 @@ constexpr int kStreamMinInputs = 4;
 //    threads then fits once per SM and the rows would run in two waves;
 //    448-thread CTAs fit twice (measured at H = 7168: m = 256-304 runs
 //    1.1-1.3x faster with 2, while from 1024 rows 1 pack per thread is up
-//    to 1.2x faster for 1-3 inputs).  Either way a CTA stays within
+//    to 1.2x faster for 1-3 inputs; with 4 or more inputs 2 packs stay
+//    better, 1.07x at n = 4, H = 4096).  Either way a CTA stays within
 //    1024 / vpt threads.
-static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int force_vpt,
-                          ar_plan_t *pl) {
+static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_cluster,
+                          int force_vpt, ar_plan_t *pl) {
   int S = 1;
   while (S < kMaxClusterCtas && (P + S - 1) / S > kMaxPacksPerCta) S *= 2;
   if (m < 32)
@@ -229,6 +230,7 @@ static void plan_register(int64_t m, int64_t P, int sms, int force_cluster, int 
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
   if (m >= 256 && m < 1024 && per_cta > 512) vpt = 2;
+  if (m >= 1024 && inputs >= 4) vpt = 2;
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
@@ -328,13 +330,16 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
   const bool shape_forced = fc != 0 || fv != 0;
+  // With exactly 4 inputs and rows of <= 512 packs the register kernel (2
+  // packs per thread) beat the stream kernel by 7-9 % at 1024 and 16384 rows.
+  const bool stream_shape = inputs > kStreamMinInputs || (inputs == kStreamMinInputs && P > 512);
   const bool want_stream =
       fk == AR_KERNEL_STREAM || (fk == AR_KERNEL_AUTO && !shape_forced &&
-                                 m >= stream_min_rows(sms) && inputs >= kStreamMinInputs);
+                                 m >= stream_min_rows(sms) && stream_shape);
   if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin,
                                    fk == AR_KERNEL_STREAM ? force : nullptr, pl))) {
     if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
-    plan_register(m, P, sms, fc, fv, pl);
+    plan_register(m, P, inputs, sms, fc, fv, pl);
     const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;
     if (per_cta > kMaxPacksPerCta) return AR_ERR_ARG;  // forced shape too small
   }

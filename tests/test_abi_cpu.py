@@ -170,6 +170,10 @@ def test_plan_spreads_small_batches(arlib):
     assert arlib.ar_get_plan(4, 256, 4096, 1, sm_count=152)["vpt"] == 1
     # few inputs, many rows: register kernel, one pack per thread
     assert arlib.ar_get_plan(2, 16384, 7168, 1, sm_count=152)["vpt"] == 1
+    # 4 inputs with short rows: register kernel, two packs per thread
+    p = arlib.ar_get_plan(4, 16384, 4096, 1, sm_count=152)
+    assert p["kernel"] == 1 and p["vpt"] == 2
+    assert arlib.ar_get_plan(4, 16384, 7168, 1, sm_count=152)["kernel"] == 2
     # stage 2 of two-stage (one input) stays on the register kernel
     assert arlib.ar_get_plan(8, 8192, 6144, 2, sm_count=152)["kernel"] == 1
     # prefill: rows alone fill the GPU; two persistent streaming CTAs per SM,
