@@ -217,9 +217,10 @@ constexpr int kStreamMinInputs = 4;
 //    threads then fits once per SM and the rows would run in two waves;
 //    448-thread CTAs fit twice (measured at H = 7168: m = 256-304 runs
 //    1.1-1.3x faster with 2, while from 1024 rows 1 pack per thread is up
-//    to 1.2x faster for 1-3 inputs; with 4 or more inputs 2 packs stay
-//    better, 1.07x at n = 4, H = 4096).  Either way a CTA stays within
-//    1024 / vpt threads.
+//    to 1.2x faster for 2-3 inputs; with 4 or more inputs 2 packs stay
+//    better, 1.07x at n = 4, H = 4096, and so do single-input epilogues
+//    with rows of more than 512 packs: stage 2 of two-stage at H = 6144 ran
+//    3.5 % faster with 2).  Either way a CTA stays within 1024 / vpt threads.
 static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_cluster,
                           int force_vpt, ar_plan_t *pl) {
   int S = 1;
@@ -229,8 +230,10 @@ static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_c
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
-  if (m >= 256 && m < 1024 && per_cta > 512) vpt = 2;
-  if (m >= 1024 && inputs >= 4) vpt = 2;
+  if (m >= 1024)
+    vpt = (inputs >= 4 || (inputs == 1 && per_cta > 512)) ? 2 : 1;
+  else if (m >= 256 && per_cta > 512)
+    vpt = 2;
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
