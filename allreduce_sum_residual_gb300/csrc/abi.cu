@@ -203,6 +203,12 @@ static int select_mode(int n, int64_t m, int64_t H) {
 static int64_t stream_min_rows(int sms) {
   return 4 * static_cast<int64_t>(sms) > 1024 ? 4 * static_cast<int64_t>(sms) : 1024;
 }
+
+// With 5 or more inputs the stream kernel already wins at mid sizes (the
+// mid-size sweep, m = 128 .. 768, n = 8): from 512 rows at every H (4-7 %),
+// and from 256 rows once a row is >= 1024 packs (H >= 8192), where the
+// register kernel's 512-1024-thread CTAs fit once per SM (up to 1.4x).
+static int64_t stream_min_rows_many_inputs(int64_t P) { return P >= 1024 ? 256 : 512; }
 constexpr int kStreamMinInputs = 4;
 
 // Register kernel: launch shape for m rows of P packs.  Set from the GB300
@@ -234,6 +240,8 @@ static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_c
     vpt = (inputs >= 4 || (inputs == 1 && per_cta > 512)) ? 2 : 1;
   else if (m >= 256 && per_cta > 512)
     vpt = 2;
+  else if (m >= 384 && inputs >= 4)
+    vpt = 2;  // n = 4 / 8 at H = 4096, m = 384-512: 6-20 % faster than 1
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
@@ -336,9 +344,11 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   // With exactly 4 inputs and rows of <= 512 packs the register kernel (2
   // packs per thread) beat the stream kernel by 7-9 % at 1024 and 16384 rows.
   const bool stream_shape = inputs > kStreamMinInputs || (inputs == kStreamMinInputs && P > 512);
+  const int64_t min_rows =
+      inputs > kStreamMinInputs ? stream_min_rows_many_inputs(P) : stream_min_rows(sms);
   const bool want_stream =
-      fk == AR_KERNEL_STREAM || (fk == AR_KERNEL_AUTO && !shape_forced &&
-                                 m >= stream_min_rows(sms) && stream_shape);
+      fk == AR_KERNEL_STREAM ||
+      (fk == AR_KERNEL_AUTO && !shape_forced && m >= min_rows && stream_shape);
   if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin,
                                    fk == AR_KERNEL_STREAM ? force : nullptr, pl))) {
     if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;

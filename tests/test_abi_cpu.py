@@ -174,6 +174,11 @@ def test_plan_spreads_small_batches(arlib):
     p = arlib.ar_get_plan(4, 16384, 4096, 1, sm_count=152)
     assert p["kernel"] == 1 and p["vpt"] == 2
     assert arlib.ar_get_plan(4, 16384, 7168, 1, sm_count=152)["kernel"] == 2
+    # many inputs at mid sizes: stream from 512 rows (256 for rows >= 1024 packs)
+    assert arlib.ar_get_plan(8, 511, 7168, 1, sm_count=152)["kernel"] == 1
+    assert arlib.ar_get_plan(8, 512, 7168, 1, sm_count=152)["kernel"] == 2
+    assert arlib.ar_get_plan(8, 256, 8192, 1, sm_count=152)["kernel"] == 2
+    assert arlib.ar_get_plan(4, 512, 4096, 1, sm_count=152)["vpt"] == 2
     # stage 2 of two-stage (one input) stays on the register kernel
     assert arlib.ar_get_plan(8, 8192, 6144, 2, sm_count=152)["kernel"] == 1
     # prefill: rows alone fill the GPU; two persistent streaming CTAs per SM,
