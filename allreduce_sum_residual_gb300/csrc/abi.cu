@@ -191,15 +191,15 @@ static int select_mode(int n, int64_t m, int64_t H) {
   return m <= one_stage_max_rows(n, H) ? AR_MODE_ONE_STAGE : AR_MODE_TWO_STAGE;
 }
 
-// The stream kernel takes over from this many rows on, when the epilogue
-// has at least kStreamMinInputs inputs.  Measured on GB300 (the bench's
-// kernels mode, one-stage, cold, n in {1, 2, 3, 4, 8, 16}, H in {4096,
-// 7168}, m in {304, 1024, 4096, 16384}): from 1024 rows on the stream
-// kernel was fastest for n = 8 (up to 7.18 TB/s) and n = 16 (at H = 4096),
-// at 304 rows the register kernel with 2 packs per thread won; with 1-3
-// inputs the register kernel with one pack per thread won at every size (up
-// to 7.19 TB/s at n = 3), and with one input (stage 2 of two-stage) the
-// ring's tiles are too small to pay for it.
+// When the stream kernel takes over (kernels and mid-size sweeps on GB300,
+// one-stage, cold buffers, n in {1, 2, 3, 4, 8, 16}, H = 4096 .. 8192,
+// m = 128 .. 16384):
+//  * 1-3 inputs never: the register kernel won at every size (up to 7.19
+//    TB/s at n = 3); with one input (stage 2 of two-stage) the ring's tiles
+//    are too small to pay for it;
+//  * 4 inputs from 1024 rows (and not for rows of <= 512 packs, where the
+//    register kernel with 2 packs per thread was 7-9 % faster);
+//  * 5 or more inputs from stream_min_rows_many_inputs (below).
 static int64_t stream_min_rows(int sms) {
   return 4 * static_cast<int64_t>(sms) > 1024 ? 4 * static_cast<int64_t>(sms) : 1024;
 }
