@@ -226,3 +226,17 @@ def test_reduce_scatter_store_checks_arguments(arlib):
     # one pack spread over 4 ranks: ranks 1..3 have empty slices and launch nothing
     for r in (1, 2, 3):
         assert call(P, 2, 8, r, 4, T, None) == OK
+
+
+def test_binding_fails_loudly_without_the_library(tmp_path):
+    """No CPU or torch fallback: with the shared library missing, the first
+    call raises instead of computing anything."""
+    code = ("import allreduce_sum_residual_gb300 as arn\n"
+            f"arn.LIB_PATH = {str(tmp_path / 'missing.so')!r}\n"
+            "try:\n    arn.ar_select_mode(8, 1, 7168)\nexcept RuntimeError as e:\n"
+            "    print('raised:', 'not built' in str(e))\nelse:\n    print('no error')\n")
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                       timeout=120)
+    assert r.stdout.strip() == "raised: True", r.stdout + r.stderr

@@ -150,6 +150,17 @@ def test_ragged_and_extreme_shapes(m, H, mode):
     check_full(device_inputs(w, m), mode, f"m={m} H={H}/{mode}")
 
 
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_many_rows_of_a_very_wide_hidden_size(mode):
+    """H = 65536 (beyond the stream kernel) at 600 rows: register kernel,
+    8-CTA clusters of 2 packs per thread; compared on sampled rows."""
+    w = synth.Workload("wide", n=5, H=65536, ms=(600,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, 600)
+    p = arn.ar_get_plan(5, 600, 65536, mode)
+    assert p["kernel"] == arn.AR_KERNEL_REGISTER and p["cluster"] == 8
+    check_sampled(inp, mode, f"wide/{mode}", k=24)
+
+
 def guarded(m, H):
     """An [m, H] bf16 view inside a buffer with 4 KiB guard bands each side,
     every guard element holding the pattern 0x5A5A."""
