@@ -71,7 +71,16 @@ def test_two_stage_workload(m, mode):
 @pytest.mark.parametrize("mode", ["one_stage", "two_stage", "auto"])
 def test_prefill_full(mode):
     w = synth.PREFILL
-    check_full(device_inputs(w, w.ms[0]), mode, f"prefill/{mode}")
+    same = check_full(device_inputs(w, w.ms[0]), mode, f"prefill/{mode}")
+    # fp32 + rsqrtf against the fp64 oracle: beyond the tolerance, almost
+    # every output rounds to the very same bf16
+    assert same >= 0.999, f"only {same:.5f} of out bit-identical to the oracle"
+
+
+@pytest.mark.parametrize("m", [1, 16])
+def test_decode_out_mostly_bit_identical(m):
+    same = check_full(device_inputs(synth.DECODE, m), "auto", f"decode m={m}")
+    assert same >= 0.999, f"only {same:.5f} of out bit-identical to the oracle"
 
 
 @pytest.mark.parametrize("w", synth.SWEEP, ids=lambda w: w.name)
