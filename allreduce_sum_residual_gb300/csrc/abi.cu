@@ -434,7 +434,7 @@ static cudaError_t launch_stream(const void *const *inputs, int n, const void *r
 static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n,
                                const void *residual, const void *weight, float eps, int64_t m,
                                int64_t H, void *out, void *residual_out, float *sum_out,
-                               const ar_plan_t &pl) {
+                               const ar_plan_t &pl, int *status) {
   std::memset(a, 0, sizeof *a);
   for (int k = 0; k < n; ++k) a->p[k] = static_cast<const uint4 *>(inputs[k]);
   a->res = static_cast<const uint4 *>(residual);
@@ -447,6 +447,8 @@ static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n
   a->per_cta = static_cast<int>((a->P + pl.cluster - 1) / pl.cluster);
   a->H = static_cast<float>(H);
   a->eps = eps;
+  a->wait_limit_ns = kWaitLimitNs;
+  a->status = status;
 }
 
 static int run(const void *const *partials, int n, const void *residual, const void *weight,
@@ -474,7 +476,7 @@ static int run(const void *const *partials, int n, const void *residual, const v
     } else {
       EpilogueArgs a;
       fill_epilogue_args(&a, inputs, count, residual, weight, eps, m, H, out, residual_out,
-                         sum_out, pl);
+                         sum_out, pl, d->status);
       e = launch_epilogue(a, count, pl, after_prior, s);
     }
     return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
@@ -547,7 +549,8 @@ int two_stage_with_temp(const void *const *partials, int n, const void *residual
                       d->status, true, s);
   } else {
     EpilogueArgs a;
-    fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl);
+    fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                       d->status);
     e = launch_epilogue(a, 1, pl, true, s);
   }
   return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;

@@ -31,6 +31,8 @@ struct EpilogueArgs {
   float eps;
   int early_reads;               // weight and residual may be read before the
                                  // wait on the previous grid (stage 2 only)
+  uint64_t wait_limit_ns;        // bound of the cluster-exchange wait
+  int *status;                   // device status word (AR_ERR_TIMEOUT on timeout)
 };
 
 // Kernel parameters of stage 1 (flat reduce of every pack across ranks).
@@ -86,14 +88,22 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // Sum of `v` over the CTA, returned to every thread.  `scratch` holds 33
-// floats.  Butterfly within each warp, one slot per warp, then warp 0 folds
-// the slots (the square-sum order is not part of the bit-exact contract).
+// floats and is used once per kernel.  Butterfly within each warp, one slot
+// per warp; with up to 8 warps every thread then adds the slots itself (one
+// barrier), with more warp 0 folds them and publishes the total (two
+// barriers, fewer shared-memory reads per thread).  The square-sum order is
+// not part of the bit-exact contract.
 __device__ __forceinline__ float block_sum(float v, float *scratch) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nwarps = (blockDim.x + 31) >> 5;
   v = warp_sum(v);
   if (lane == 0) scratch[warp] = v;
   __syncthreads();
+  if (nwarps <= 8) {
+    float t = 0.f;
+    for (int i = 0; i < nwarps; ++i) t += scratch[i];
+    return t;
+  }
   if (warp == 0) {
     float t = lane < nwarps ? scratch[lane] : 0.f;
     t = warp_sum(t);
@@ -139,31 +149,89 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
   return r;
 }
 
-// Cluster-wide barrier; release/acquire order the distributed-shared-memory
-// writes before it against the reads after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+// Split cluster barrier.  arrive.release at kernel start (after this CTA
+// has initialised what its peers will touch), wait.acquire right before the
+// first access to a peer's shared memory -- which must not happen before
+// every CTA of the cluster runs.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
 
-// Split phase of the cluster barrier with no memory ordering: arrive at the
-// start of the kernel, wait right before the first access to a peer's shared
-// memory -- which must not happen before every CTA of the cluster runs.
-__device__ __forceinline__ void cluster_arrive_relaxed() {
-  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void cluster_wait() {
-  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
+// --- mbarriers (PTX) ---------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Write a float into the shared memory of CTA `rank` of this cluster, at the
-// address that `local` has in this CTA.
-__device__ __forceinline__ void st_dsmem(float *local, uint32_t rank, float v) {
-  uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait until phase `parity` of `bar` completes, for at most limit_ns.  On
+// timeout: record AR_ERR_TIMEOUT, raise the CTA's abort flag, return false.
+// Also returns false (without waiting) once another thread raised abort.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  volatile int *abort_flag, uint64_t limit_ns,
+                                                  int *status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort_flag = 1;
+      if (status) atomicExch(status, AR_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Store a float into the shared memory of CTA `rank` of this cluster, at the
+// address that `local_slot` has in this CTA, completing 4 transaction bytes
+// on that CTA's mbarrier at the address of `local_bar` (st.async): the
+// receiver learns of the value by waiting on its own barrier, without a
+// cluster-wide barrier.
+__device__ __forceinline__ void st_async_remote_f32(float *local_slot, uint32_t rank, float v,
+                                                    uint64_t *local_bar) {
+  uint32_t ra, rb;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_addr(local_slot)), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_addr(local_bar)), "r"(rank));
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(ra),
+               "f"(v), "r"(rb)
+               : "memory");
 }
 
 }  // namespace arn

@@ -13,11 +13,14 @@
 // it over the ranks in order: the sum does not depend on S, T or VPT.
 //
 // The square sum is reduced warp -> CTA -> cluster.  In the cluster step
-// every CTA writes its total into slot q of every peer's shared memory
-// (distributed shared memory), one cluster barrier publishes the writes,
-// and each CTA adds slots 0..S-1 in rank order: all CTAs of a row derive
-// the same scale, and no CTA touches a peer's memory after the barrier, so
-// none has to wait for the others before it exits.
+// every CTA sends its total into slot q of every peer's shared memory with
+// st.async, which completes 4 bytes on the receiver's mbarrier; each CTA
+// waits on its own barrier for the S totals (a one-sided wait, no cluster-
+// wide barrier) and adds slots 0..S-1 in rank order, so all CTAs of a row
+// derive the same scale.  A CTA leaves only after all S totals reached it,
+// so no peer writes into an exited CTA.  The wait is bounded: on timeout
+// it records AR_ERR_TIMEOUT in the device status word and goes on (the
+// outputs of that call are then not valid).
 #pragma once
 
 #include "common.cuh"
@@ -48,6 +51,8 @@ __global__ void __launch_bounds__(1024 / VPT)
 k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   __shared__ float red[33];
   __shared__ float cta_totals[kMaxClusterCtas];
+  __shared__ uint64_t totals_bar;  // completes when the S cluster totals have arrived
+  __shared__ int totals_abort;
 
   const uint32_t S = cluster_nctarank();       // 1 unless launched as a cluster
   const uint32_t q = cluster_ctarank();
@@ -56,7 +61,14 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   const int c1 = min(a.P, c0 + a.per_cta);
   const int64_t base = row * static_cast<int64_t>(a.P);
   const int T = blockDim.x;
-  if (S > 1) cluster_arrive_relaxed();  // this CTA runs (see the cluster step)
+  if (S > 1) {
+    if (threadIdx.x == 0) {
+      mbar_init(&totals_bar, 1);
+      totals_abort = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    cluster_arrive_release();  // this CTA runs and its barrier is ready for its peers
+  }
 
   // Loads first: n partials, the residual and the weight of every pack this
   // thread owns.  Nothing is stored before the last load is issued.  In
@@ -108,9 +120,10 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
 
   float total = block_sum(ss, red);
   if (S > 1) {
-    cluster_wait();  // every CTA of the cluster has started: peers' memory is live
-    if (threadIdx.x < S) st_dsmem(&cta_totals[q], threadIdx.x, total);
-    cluster_sync();
+    cluster_wait_acquire();  // every peer runs and has initialised its barrier
+    if (threadIdx.x == 0) mbar_arrive_expect_tx(&totals_bar, S * static_cast<uint32_t>(sizeof(float)));
+    if (threadIdx.x < S) st_async_remote_f32(&cta_totals[q], threadIdx.x, total, &totals_bar);
+    mbar_wait_bounded(&totals_bar, 0, &totals_abort, a.wait_limit_ns, a.status);
     total = 0.f;
     for (uint32_t k = 0; k < S; ++k) total += cta_totals[k];
   }
