@@ -215,9 +215,10 @@ constexpr int kStreamMinInputs = 4;
 // launch-shape sweep (the bench's shapes mode: decode n = 8 and mid-size
 // n = 4 at H = 7168, every cluster size x packs per thread, hot and cold):
 //  * cluster S: the fewest CTAs per row that hold a row slice in registers
-//    (<= 1024 packs per CTA); below 32 rows, a row is spread over 8 CTAs
-//    (each keeping >= 32 packs) -- 8 beat 16, 4 and 1 at m <= 16 -- while
-//    from 32 rows on one CTA per row was fastest;
+//    (<= 1024 packs per CTA); below 64 rows, a row is spread over 8 CTAs
+//    (each keeping >= 32 packs) -- 8 matched or beat 16, 4, 2 and 1 at
+//    m <= 32 once the cluster exchange became one st.async per CTA pair --
+//    while from 64 rows one CTA per row was as fast or faster;
 //  * vpt: 1 pack per thread (the most loads in flight per CTA), except 2
 //    for 256 .. 1023 rows of more than 512 packs: a CTA of up to 1024
 //    threads then fits once per SM and the rows would run in two waves;
@@ -231,7 +232,7 @@ static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_c
                           int force_vpt, ar_plan_t *pl) {
   int S = 1;
   while (S < kMaxClusterCtas && (P + S - 1) / S > kMaxPacksPerCta) S *= 2;
-  if (m < 32)
+  if (m < 64)
     while (S < 8 && (P + 2 * S - 1) / (2 * S) >= 32) S *= 2;
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;

@@ -162,10 +162,10 @@ def test_plan_covers_every_pack(arlib, n, m, H, mode):
 
 
 def test_plan_spreads_small_batches(arlib):
-    # decode: a row of H = 7168 spreads over an 8-CTA cluster below 32 rows
-    for m in (1, 4, 16, 31):
+    # decode: a row of H = 7168 spreads over an 8-CTA cluster below 64 rows
+    for m in (1, 4, 16, 32, 63):
         assert arlib.ar_get_plan(8, m, 7168, 1, sm_count=152)["cluster"] == 8
-    assert arlib.ar_get_plan(4, 32, 7168, 1, sm_count=152)["cluster"] == 1
+    assert arlib.ar_get_plan(4, 64, 7168, 1, sm_count=152)["cluster"] == 1
     assert arlib.ar_get_plan(4, 256, 7168, 1, sm_count=152)["vpt"] == 2
     assert arlib.ar_get_plan(4, 256, 4096, 1, sm_count=152)["vpt"] == 1
     # few inputs, many rows: register kernel, one pack per thread
