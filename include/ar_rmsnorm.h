@@ -247,6 +247,10 @@ int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
  * m*H the two-stage path will see) on `device`.  Allocates with cudaMalloc,
  * so call it before any graph capture.  Growing replaces the old buffer
  * (after a device synchronisation); a smaller request keeps the current one.
+ * All two-stage calls on a device share this one buffer: two-stage calls
+ * that may overlap on the GPU (different streams without ordering between
+ * them) race on it, so order them, e.g. on one stream.  One-stage calls use
+ * no workspace and have no such restriction.
  */
 int ar_reserve_workspace(int64_t max_elems, int device);
 
