@@ -573,12 +573,16 @@ def cpu_baseline(synth_inp, n, H, eps, two_stage, budget_s=10.0):
     dt = time.perf_counter() - t
     rows = int(min(m, max(probe, probe * budget_s / max(dt, 1e-6))))
     parts, res, w = rows_bits(rows)
-    t = time.perf_counter()
-    oracle.ar_rmsnorm(parts, res, w, eps, two_stage=two_stage, threads=threads)
-    dt = time.perf_counter() - t
-    return {"value": round(algo_bytes(n, rows, H) / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
-            "kind": "oracle",
-            "sample": f"first {rows} of {m} rows of the workload, one oracle pass, "
+    # whole passes over the sample until about budget_s of time has passed
+    passes, dt = 0, 0.0
+    while dt < budget_s or passes == 0:
+        t = time.perf_counter()
+        oracle.ar_rmsnorm(parts, res, w, eps, two_stage=two_stage, threads=threads)
+        dt += time.perf_counter() - t
+        passes += 1
+    return {"value": round(passes * algo_bytes(n, rows, H) / dt / 1e9, 4), "unit": "GB/s",
+            "cores": threads, "kind": "oracle",
+            "sample": f"first {rows} of {m} rows of the workload, {passes} oracle passes, "
                       f"{threads} threads, {dt:.2f} s"}
 
 
