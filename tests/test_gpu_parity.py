@@ -365,6 +365,33 @@ def test_graph_capture_and_replay():
     compare((out, rout, None), oracle_rows(inp, None, True), "graph replay")
 
 
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_stream_kernel_in_a_graph_matches_eager(mode):
+    """The persistent stream kernel (and two-stage) captured in a CUDA graph
+    gives the same bits as the same call launched eagerly."""
+    w = synth.Workload("graph", n=8, H=6144, ms=(1536,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, 1536)
+    if mode == "one_stage":
+        assert arn.ar_get_plan(8, 1536, 6144, 1)["kernel"] == arn.AR_KERNEL_STREAM
+    ref_out, ref_rout = arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, mode=mode)
+    s = torch.cuda.Stream()
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for _ in range(3):
+            arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, out=out,
+                           residual_out=rout, mode=mode)
+    out.zero_()
+    rout.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(rout.view(torch.int16), ref_rout.view(torch.int16))
+    assert arn.ar_device_status(0) == arn.AR_OK
+
+
 def test_non_default_stream():
     w = synth.DECODE
     inp = device_inputs(w, 4)
