@@ -4,17 +4,16 @@ lightseekorg/tokenspeed #968 "perf(comm): add opt-in Triton AR+RMSNorm
 backend", review comments on state creation: when setup (an allocation, a
 runtime call) fails on one rank only, that rank falls back while its peers
 keep the fused path, the group splits between two collectives and hangs.
-The cure named there is to exchange a success flag so that every rank
-decides on the fallback together, including when the allocation itself
-fails.
+The review's remedy is for the ranks to share whether their setup worked,
+so that all of them take the same path -- the allocation included.
 
 Here the setup that can fail rank-locally is the reservation of the
 two-stage workspace.  ``reserve_two_stage_workspace`` has every rank try it,
 then all-reduces (MIN) a success flag; if any rank failed, every rank
 releases what it reserved and returns False, so the whole group uses the
 one-stage path (which needs no workspace).  The decision is made once, at
-setup, outside graph capture, and the caller keeps it (a permanent decline,
-as the same review asks for).
+setup, outside graph capture, and the caller keeps it for good (the same
+review asks that a failed setup not be retried on every call).
 """
 from typing import Callable, Optional
 

@@ -2,17 +2,17 @@
 // the n ranks, rounded to bf16 into the temporary buffer.
 //
 // ROCm/aiter #3817 "perf: optimize fused AllReduce + RMSNorm
-// (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: each
-// thread reduces one pack across all input ranks in fp32, downcasts the sum
-// to bf16 and stores it; no shared memory and no block barrier; the rank
-// order ptrs[0..n-1] is kept.  Stage-1 launch config: 256-thread blocks.
+// (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: one
+// thread owns one 16-byte pack, sums it over the ranks in fp32 in pointer
+// order, rounds the sum to bf16 and stores it, with neither shared memory
+// nor a block barrier.  Stage-1 launch config: 256-thread blocks.
 //
 // A launch covers the pack range [begin, end) and stores every sum into
 // ndst destinations at the same position.  The two-stage path uses the
 // whole range and one destination (this GPU's temporary).  One rank of a
 // reduce-scatter uses its slice and one destination per rank -- the page's
-// "writes it to every rank's temporary buffer directly"; across GPUs those
-// would be peer-mapped buffers.  The grid is a multiple of the SM count and
+// stores straight into each rank's temporary; across GPUs those would be
+// peer-mapped buffers.  The grid is a multiple of the SM count and
 // strides over the range; each step of a thread handles U packs 256 apart,
 // issuing all U*n loads before the first add.
 #include "epilogue.cuh"

@@ -17,7 +17,7 @@
  * order partials[0], partials[1], ..., partials[n-1], so it is bit-exact and
  * independent of the launch shape (ROCm/aiter #3817 "perf: optimize fused
  * AllReduce + RMSNorm (custom_all_reduce)", Technical Details, 2stage,
- * reduce-scatter: the reduce order over ptrs[0..ngpus-1] is kept).
+ * reduce-scatter: the sum follows the order of the rank pointers).
  *
  * Two paths compute it:
  *   one-stage  a single kernel, one pass over memory (same page, Technical
@@ -31,10 +31,9 @@
  *              are those of s' = bf16(s) in place of s.
  *
  * Data layout: every tensor is bf16, contiguous and row-major; partials,
- * residual, out and residual_out are [m, H] and weight is [H]
- * (contiguous bf16 (tokens, hidden) tensors with a bf16 weight, the scope
- * validated in lightseekorg/tokenspeed #968 "perf(comm): add opt-in Triton
- * AR+RMSNorm backend", Summary).
+ * residual, out and residual_out are [m, H] and weight is [H] -- the
+ * scope validated in lightseekorg/tokenspeed #968 "perf(comm): add opt-in
+ * Triton AR+RMSNorm backend", Summary.
  * Every pointer must be 16-byte aligned and H a multiple of 8 (one 16-byte
  * pack = 8 bf16).
  *
@@ -179,8 +178,8 @@ int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count,
  * min((rank+1)*S, count/8)) with S = ceil(count/8 / world) -- are reduced
  * across the n partials (fp32, rank order) and bf16(sum) is stored at the
  * same positions of every buffer temps[0 .. world-1] (ROCm/aiter #3817,
- * Technical Details, 2stage, reduce-scatter: each pack is reduced and
- * written "to every rank's temporary buffer directly").  Once all `world`
+ * Technical Details, 2stage, reduce-scatter: each reduced pack is stored
+ * straight into the temporary of every rank).  Once all `world`
  * ranks have run it, and synchronised, every temp holds the whole bf16 sum
  * and stage 2 (ar_load_rmsnorm) can run on any of them.
  *   partials  host array of n device pointers, count bf16 each.

@@ -12,16 +12,16 @@
  *      every add an IEEE fp32 add rounded to nearest even, strictly in the
  *      rank order of the pointer array.
  *      Source: ROCm/aiter #3817 "perf: optimize fused AllReduce + RMSNorm
- *      (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: each
- *      pack is reduced across all input ranks in fp32 and the reduce order
- *      over ptrs[0..ngpus-1] is kept, which makes the sum bit-reproducible.
+ *      (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: the
+ *      sum of every 16-byte pack is taken in fp32 over the ranks, always in
+ *      the order of the pointer array, so it comes out the same bits.
  *   2. two-stage only: t = bf16_rne(acc) and acc := f32(t).  Same section:
- *      stage 1 "downcasts the result to bf16" before it is written to the
- *      temporary buffer that stage 2 (local_device_load_rmsnorm) loads.
+ *      stage 1 rounds the sum to bf16 before storing it in the temporary
+ *      buffer that stage 2 (local_device_load_rmsnorm) loads.
  *   3. r = acc + f32(residual[i,j]) in fp32; residual_out = bf16_rne(r).
  *      The residual enters after all n partials (AllReduce, then residual add).
- *   4. RMSNorm, as named by the title of aiter #3817 and its stage-2 section
- *      ("RMSNorm square-sum reduction"), in its textbook form:
+ *   4. RMSNorm, as named by the title of aiter #3817 and by its stage-2 section
+ *      on the RMSNorm's sum of squares, in its textbook form:
  *      ss = sum_j r_j^2, inv = 1/sqrt(ss/H + eps), out = bf16_rne(r_j*inv*w_j).
  *      The pages fix no precision for this part, so it runs in fp64; only
  *      the final value is rounded (once) to bf16.

@@ -85,7 +85,7 @@ def _consensus_rank(rank, world, port, fail_rank, q):
 
     def reserve(elems, device):
         if rank == fail_rank:
-            raise MemoryError("injected rank-local allocation failure")
+            raise MemoryError("allocation failure injected on this rank")
         held.append(elems)
 
     def release(device):
