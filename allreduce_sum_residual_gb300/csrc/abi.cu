@@ -19,6 +19,10 @@ EpilogueKernel epilogue_kernel_group0(int n, int vpt_log2);
 EpilogueKernel epilogue_kernel_group1(int n, int vpt_log2);
 EpilogueKernel epilogue_kernel_group2(int n, int vpt_log2);
 EpilogueKernel epilogue_kernel_group3(int n, int vpt_log2);
+EpilogueKernel epilogue_cluster_kernel_group0(int n, int vpt_log2);
+EpilogueKernel epilogue_cluster_kernel_group1(int n, int vpt_log2);
+EpilogueKernel epilogue_cluster_kernel_group2(int n, int vpt_log2);
+EpilogueKernel epilogue_cluster_kernel_group3(int n, int vpt_log2);
 cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream);
 StreamKernel stream_kernel_group0(int n, int vpt_log2);
 StreamKernel stream_kernel_group1(int n, int vpt_log2);
@@ -31,9 +35,15 @@ constexpr int kAssumedSmemOptin = 232448;         // sm_100-class opt-in per CTA
 
 static int vpt_log2(int vpt) { return vpt == 1 ? 0 : vpt == 2 ? 1 : vpt == 4 ? 2 : vpt == 8 ? 3 : -1; }
 
-EpilogueKernel epilogue_kernel(int n, int vpt) {
+EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered) {
   const int l = vpt_log2(vpt);
   if (n < 1 || n > AR_MAX_RANKS || l < 0) return nullptr;
+  if (clustered) switch ((n - 1) / 4) {
+      case 0: return epilogue_cluster_kernel_group0(n, l);
+      case 1: return epilogue_cluster_kernel_group1(n, l);
+      case 2: return epilogue_cluster_kernel_group2(n, l);
+      default: return epilogue_cluster_kernel_group3(n, l);
+    }
   switch ((n - 1) / 4) {
     case 0: return epilogue_kernel_group0(n, l);
     case 1: return epilogue_kernel_group1(n, l);
@@ -102,7 +112,7 @@ static DeviceState *current_device(int *status) {
     // Rows split over up to 16 CTAs need the non-portable cluster size.
     for (int n = 1; n <= AR_MAX_RANKS; ++n)
       for (int vpt = 1; vpt <= 8; vpt *= 2) {
-        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(epilogue_kernel(n, vpt)),
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(epilogue_kernel(n, vpt, true)),
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
           cudaGetLastError();
           *status = AR_ERR_CUDA;
@@ -390,7 +400,7 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
   cfg.numAttrs = na;
   EpilogueArgs args = a;
   args.early_reads = after_prior ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt), args);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt, pl.cluster > 1), args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -46,7 +46,11 @@ __device__ __forceinline__ void sum_pack_in_rank_order(const uint4 *const (&p)[A
   }
 }
 
-template <int N, int VPT>
+// CL: launched as a thread-block cluster (S > 1 CTAs per row).  A one-CTA-
+// per-row launch uses the CL = false instantiation, which has no exchange
+// code and so keeps the register count (and the CTAs per SM) of a plain
+// row kernel.
+template <int N, int VPT, bool CL>
 __global__ void __launch_bounds__(1024 / VPT)
 k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   __shared__ float red[33];
@@ -54,14 +58,14 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   __shared__ uint64_t totals_bar;  // completes when the S cluster totals have arrived
   __shared__ int totals_abort;
 
-  const uint32_t S = cluster_nctarank();       // 1 unless launched as a cluster
-  const uint32_t q = cluster_ctarank();
+  const uint32_t S = CL ? cluster_nctarank() : 1u;
+  const uint32_t q = CL ? cluster_ctarank() : 0u;
   const int64_t row = blockIdx.x / S;
   const int c0 = static_cast<int>(q) * a.per_cta;
   const int c1 = min(a.P, c0 + a.per_cta);
   const int64_t base = row * static_cast<int64_t>(a.P);
   const int T = blockDim.x;
-  if (S > 1) {
+  if constexpr (CL) {
     if (threadIdx.x == 0) {
       mbar_init(&totals_bar, 1);
       totals_abort = 0;
@@ -119,7 +123,7 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   }
 
   float total = block_sum(ss, red);
-  if (S > 1) {
+  if constexpr (CL) {
     cluster_wait_acquire();  // every peer runs and has initialised its barrier
     if (threadIdx.x == 0) mbar_arrive_expect_tx(&totals_bar, S * static_cast<uint32_t>(sizeof(float)));
     if (threadIdx.x < S) st_async_remote_f32(&cta_totals[q], threadIdx.x, total, &totals_bar);
@@ -142,8 +146,9 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   }
 }
 
-// Kernel pointer for (n, vpt); n in [1, AR_MAX_RANKS], vpt in {1, 2, 4, 8}.
+// Kernel pointer for (n, vpt, clustered); n in [1, AR_MAX_RANKS], vpt in
+// {1, 2, 4, 8}.
 using EpilogueKernel = void (*)(EpilogueArgs);
-EpilogueKernel epilogue_kernel(int n, int vpt);
+EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered);
 
 }  // namespace arn

@@ -1,0 +1,16 @@
+// Instantiations of the fused epilogue kernel for n = 5 .. 8 partials,
+// launched with a thread-block cluster per row.
+// (Split over several translation units so that they compile in parallel.)
+#include "epilogue.cuh"
+
+namespace arn {
+
+#define ARN_ROW(N) {&k_fused_epilogue<N, 1, true>, &k_fused_epilogue<N, 2, true>, \
+                    &k_fused_epilogue<N, 4, true>, &k_fused_epilogue<N, 8, true>}
+
+EpilogueKernel epilogue_cluster_kernel_group1(int n, int vpt_log2) {
+  static const EpilogueKernel table[4][4] = {ARN_ROW(5), ARN_ROW(6), ARN_ROW(7), ARN_ROW(8)};
+  return table[n - 5][vpt_log2];
+}
+
+}  // namespace arn

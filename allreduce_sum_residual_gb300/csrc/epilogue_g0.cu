@@ -1,11 +1,12 @@
-// Instantiations of the fused epilogue kernel for n = 1 .. 4 partials.
-// (Split over four translation units so that they compile in parallel.)
+// Instantiations of the fused epilogue kernel for n = 1 .. 4 partials,
+// launched with one CTA per row.
+// (Split over several translation units so that they compile in parallel.)
 #include "epilogue.cuh"
 
 namespace arn {
 
-#define ARN_ROW(N) {&k_fused_epilogue<N, 1>, &k_fused_epilogue<N, 2>, \
-                    &k_fused_epilogue<N, 4>, &k_fused_epilogue<N, 8>}
+#define ARN_ROW(N) {&k_fused_epilogue<N, 1, false>, &k_fused_epilogue<N, 2, false>, \
+                    &k_fused_epilogue<N, 4, false>, &k_fused_epilogue<N, 8, false>}
 
 EpilogueKernel epilogue_kernel_group0(int n, int vpt_log2) {
   static const EpilogueKernel table[4][4] = {ARN_ROW(1), ARN_ROW(2), ARN_ROW(3), ARN_ROW(4)};

@@ -840,9 +840,10 @@ def run_kernels(args):
     stream = torch.cuda.Stream()
     props = torch.cuda.get_device_properties(0)
     l2 = getattr(props, "L2_cache_size", L2_BYTES_FALLBACK) or L2_BYTES_FALLBACK
-    for n in (1, 2, 3, 4, 8, 16):
-        for H in (4096, 7168):
-            for m in (304, 1024, 4096, 16384):
+    ints = lambda s: tuple(int(x) for x in s.split(","))
+    for n in ints(args.kernel_ns):
+        for H in ints(args.kernel_hs):
+            for m in ints(args.kernel_ms):
                 w = synth.Workload("k", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0)
                 set_bytes = algo_bytes(n, m, H)
                 calls = 2000 if set_bytes < 32 << 20 else 100
@@ -904,6 +905,9 @@ def main(argv=None):
     ap.add_argument("--shapes", action="store_true", help="register-kernel launch-shape sweep")
     ap.add_argument("--kernels", action="store_true", help="register vs stream kernel sweep")
     ap.add_argument("--stream-shapes", action="store_true", help="stream-kernel shape sweep")
+    ap.add_argument("--kernel-ns", default="1,2,3,4,8,16", help="--kernels: input counts")
+    ap.add_argument("--kernel-hs", default="4096,7168", help="--kernels: hidden sizes")
+    ap.add_argument("--kernel-ms", default="304,1024,4096,16384", help="--kernels: token counts")
     ap.add_argument("--quick", action="store_true", help="shorter latency table and baselines")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
