@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "epilogue.cuh"
+#include "plan_table.cuh"
 #include "stream_epilogue.cuh"
 
 // The device status word: AR_OK, or AR_ERR_TIMEOUT after a bounded wait in a
@@ -201,25 +202,80 @@ static int select_mode(int n, int64_t m, int64_t H) {
   return m <= one_stage_max_rows(n, H) ? AR_MODE_ONE_STAGE : AR_MODE_TWO_STAGE;
 }
 
-// When the stream kernel takes over (kernels and mid-size sweeps on GB300,
-// one-stage, cold buffers, n in {1, 2, 3, 4, 8, 16}, H = 4096 .. 8192,
-// m = 128 .. 16384):
-//  * 1-3 inputs never: the register kernel won at every size (up to 7.19
-//    TB/s at n = 3); with one input (stage 2 of two-stage) the ring's tiles
-//    are too small to pay for it;
-//  * 4 inputs from 1024 rows (and not for rows of <= 512 packs, where the
-//    register kernel with 2 packs per thread was 7-9 % faster);
-//  * 5 or more inputs from stream_min_rows_many_inputs (below).
-static int64_t stream_min_rows(int sms) {
-  return 4 * static_cast<int64_t>(sms) > 1024 ? 4 * static_cast<int64_t>(sms) : 1024;
+// Kernel choice from 64 rows on, for rows up to the table's longest (1024
+// packs, H = 8192): the lookup table of plan_table.cuh, measured on GB300.
+// For every (inputs, packs per row, rows) of its grid it holds each
+// candidate's speed as a percentage of the fastest there: the stream kernel
+// and the register kernel with 1, 2, 4 or 8 packs per thread (one-stage,
+// cold buffers, CUDA-graph timing; repeated sweeps agreed within 0.5 %).
+// No simple rule fits it: which kernel wins turns on how many CTAs of each
+// fit an SM (the register counts of each instantiation), whether the rows
+// fill a whole number of waves, and how many bytes are then in flight --
+// one more wave of a few rows can cost 25 %.  Between grid points the
+// percentages of the grid cells that bracket the shape (two columns per
+// axis where it falls between two: inputs, packs, rows) are added up and
+// the best sum wins, which prefers a candidate that is good on both sides
+// of a cliff.  Rows are first scaled to the table's SM count; rows
+// shorter than the table's shortest use its column.  Returns 0 for the
+// stream kernel, the register kernel's packs per thread, or -1 where the
+// table does not apply (fewer than 64 rows, where the register kernel
+// spreads a row over a cluster, or rows longer than the table's longest).
+constexpr int64_t kTableMinRows = 64;
+
+// The grid columns around x: [lo, hi] = [i - 1, i] between two columns,
+// [i, i] on a column or beyond either end.
+template <int K>
+static void bracket(const int (&grid)[K], double x, int *lo, int *hi) {
+  if (x <= grid[0]) {
+    *lo = *hi = 0;
+    return;
+  }
+  for (int i = 0; i < K; ++i) {
+    if (x == grid[i]) {
+      *lo = *hi = i;
+      return;
+    }
+    if (x < grid[i]) {
+      *lo = i - 1;
+      *hi = i;
+      return;
+    }
+  }
+  *lo = *hi = K - 1;
 }
 
-// With 5 or more inputs the stream kernel already wins at mid sizes (the
-// mid-size sweep, m = 128 .. 768, n = 8): from 512 rows at every H (4-7 %),
-// and from 256 rows once a row is >= 1024 packs (H >= 8192), where the
-// register kernel's 512-1024-thread CTAs fit once per SM (up to 1.4x).
-static int64_t stream_min_rows_many_inputs(int64_t P) { return P >= 1024 ? 256 : 512; }
-constexpr int kStreamMinInputs = 4;
+template <int K>
+static int last_of(const int (&grid)[K]) {
+  return grid[K - 1];
+}
+
+static int table_choice(int inputs, int64_t m, int64_t P, int sms) {
+  if (m < kTableMinRows || P > last_of(kPlanPacks)) return -1;
+  int n0, n1, p0, p1, m0, m1;
+  bracket(kPlanInputs, static_cast<double>(inputs), &n0, &n1);
+  bracket(kPlanPacks, static_cast<double>(P), &p0, &p1);
+  bracket(kPlanRows, static_cast<double>(m) * kPlanTableSms / sms, &m0, &m1);
+  int score[kPlanCandidates] = {};
+  for (int ni = n0; ni <= n1; ++ni)
+    for (int pi = p0; pi <= p1; ++pi)
+      for (int mi = m0; mi <= m1; ++mi)
+        for (int c = 0; c < kPlanCandidates; ++c) score[c] += kPlanScore[ni][pi][mi][c];
+  int best = 0;
+  for (int c = 1; c < kPlanCandidates; ++c)
+    if (score[c] > score[best]) best = c;
+  return best == 0 ? 0 : 1 << (best - 1);
+}
+
+// Rows of more than 1024 packs (beyond the table): the stream kernel for 4
+// inputs from max(4 x SMs, 1024) rows and for 5 or more from 256 rows (at
+// H = 8192 the register kernel's 1024-thread CTAs fit once per SM, up to
+// 1.4x slower than the stream kernel from 256 rows at n = 8); otherwise the
+// register kernel, a row split over a cluster.
+static bool long_rows_want_stream(int inputs, int64_t m, int sms) {
+  if (inputs < 4) return false;
+  const int64_t four_waves = 4 * static_cast<int64_t>(sms);
+  return m >= (inputs > 4 ? 256 : (four_waves > 1024 ? four_waves : 1024));
+}
 
 // Register kernel: launch shape for m rows of P packs.  Set from the GB300
 // launch-shape sweep (the bench's shapes mode: decode n = 8 and mid-size
@@ -229,17 +285,15 @@ constexpr int kStreamMinInputs = 4;
 //    (each keeping >= 32 packs) -- 8 matched or beat 16, 4, 2 and 1 at
 //    m <= 32 once the cluster exchange became one st.async per CTA pair --
 //    while from 64 rows one CTA per row was as fast or faster;
-//  * vpt: 1 pack per thread (the most loads in flight per CTA), except 2
-//    for 256 .. 1023 rows of more than 512 packs: a CTA of up to 1024
-//    threads then fits once per SM and the rows would run in two waves;
-//    448-thread CTAs fit twice (measured at H = 7168: m = 256-304 runs
-//    1.1-1.3x faster with 2, while from 1024 rows 1 pack per thread is up
-//    to 1.2x faster for 2-3 inputs; with 4 or more inputs 2 packs stay
-//    better, 1.07x at n = 4, H = 4096, and so do single-input epilogues
-//    with rows of more than 512 packs: stage 2 of two-stage at H = 6144 ran
-//    3.5 % faster with 2).  Either way a CTA stays within 1024 / vpt threads.
-static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_cluster,
-                          int force_vpt, ar_plan_t *pl) {
+//  * vpt: `table_vpt` where the lookup table gives one; otherwise (below 64
+//    rows, or rows of more than 1024 packs) 1 pack per thread, the most
+//    loads in flight per CTA, except 2 for 256 .. 1023 rows of more than
+//    512 packs a CTA (a CTA of up to 1024 threads fits once per SM and the
+//    rows would run in two waves) and for 1024 rows or more with 4 inputs
+//    or more, or one input with more than 512 packs a CTA.  Either way a
+//    CTA stays within 1024 / vpt threads.
+static void plan_register(int64_t m, int64_t P, int inputs, int force_cluster, int force_vpt,
+                          int table_vpt, ar_plan_t *pl) {
   int S = 1;
   while (S < kMaxClusterCtas && (P + S - 1) / S > kMaxPacksPerCta) S *= 2;
   if (m < 64)
@@ -247,12 +301,12 @@ static void plan_register(int64_t m, int64_t P, int inputs, int sms, int force_c
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
-  if (m >= 1024)
+  if (table_vpt > 0 && S == 1)
+    vpt = table_vpt;
+  else if (m >= 1024)
     vpt = (inputs >= 4 || (inputs == 1 && per_cta > 512)) ? 2 : 1;
   else if (m >= 256 && per_cta > 512)
     vpt = 2;
-  else if (m >= 384 && inputs >= 4)
-    vpt = 2;  // n = 4 / 8 at H = 4096, m = 384-512: 6-20 % faster than 1
   while (vpt < 8 && (per_cta + vpt - 1) / vpt > 1024 / vpt) vpt *= 2;
   if (force_vpt > 0) vpt = force_vpt;
   int threads = static_cast<int>((per_cta + vpt - 1) / vpt);
@@ -352,18 +406,14 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
   const bool shape_forced = fc != 0 || fv != 0;
-  // With exactly 4 inputs and rows of <= 512 packs the register kernel (2
-  // packs per thread) beat the stream kernel by 7-9 % at 1024 and 16384 rows.
-  const bool stream_shape = inputs > kStreamMinInputs || (inputs == kStreamMinInputs && P > 512);
-  const int64_t min_rows =
-      inputs > kStreamMinInputs ? stream_min_rows_many_inputs(P) : stream_min_rows(sms);
-  const bool want_stream =
-      fk == AR_KERNEL_STREAM ||
-      (fk == AR_KERNEL_AUTO && !shape_forced && m >= min_rows && stream_shape);
+  const int choice = table_choice(inputs, m, P, sms);
+  bool want_stream = fk == AR_KERNEL_STREAM;
+  if (fk == AR_KERNEL_AUTO && !shape_forced)
+    want_stream = choice >= 0 ? choice == 0 : long_rows_want_stream(inputs, m, sms);
   if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin,
                                    fk == AR_KERNEL_STREAM ? force : nullptr, pl))) {
     if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
-    plan_register(m, P, inputs, sms, fc, fv, pl);
+    plan_register(m, P, inputs, fc, fv, choice > 0 ? choice : 0, pl);
     const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;
     if (per_cta > kMaxPacksPerCta) return AR_ERR_ARG;  // forced shape too small
   }

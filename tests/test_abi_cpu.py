@@ -166,37 +166,112 @@ def test_plan_spreads_small_batches(arlib):
     for m in (1, 4, 16, 32, 63):
         assert arlib.ar_get_plan(8, m, 7168, 1, sm_count=152)["cluster"] == 8
     assert arlib.ar_get_plan(4, 64, 7168, 1, sm_count=152)["cluster"] == 1
-    assert arlib.ar_get_plan(4, 256, 7168, 1, sm_count=152)["vpt"] == 2
-    assert arlib.ar_get_plan(4, 256, 4096, 1, sm_count=152)["vpt"] == 1
-    # few inputs, many rows: register kernel, one pack per thread
-    assert arlib.ar_get_plan(2, 16384, 7168, 1, sm_count=152)["vpt"] == 1
-    # 4 inputs with short rows: register kernel, two packs per thread
-    p = arlib.ar_get_plan(4, 16384, 4096, 1, sm_count=152)
-    assert p["kernel"] == 1 and p["vpt"] == 2
-    assert arlib.ar_get_plan(4, 16384, 7168, 1, sm_count=152)["kernel"] == 2
-    # many inputs at mid sizes: stream from 512 rows (256 for rows >= 1024 packs)
-    assert arlib.ar_get_plan(8, 511, 7168, 1, sm_count=152)["kernel"] == 1
-    assert arlib.ar_get_plan(8, 512, 7168, 1, sm_count=152)["kernel"] == 2
-    assert arlib.ar_get_plan(8, 256, 8192, 1, sm_count=152)["kernel"] == 2
-    assert arlib.ar_get_plan(4, 512, 4096, 1, sm_count=152)["vpt"] == 2
-    # stage 2 of two-stage (one input) stays on the register kernel
-    assert arlib.ar_get_plan(8, 8192, 6144, 2, sm_count=152)["kernel"] == 1
     # prefill: rows alone fill the GPU; two persistent streaming CTAs per SM,
     # each with a 2-slot ring of 9 x 4 KB tiles (144 KB in flight per SM)
     p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 2 and p["threads"] == 288
     # 4 inputs, H = 7168: two CTAs per SM with 3 slots of 5 x 3.5 KB
     p = arlib.ar_get_plan(4, 8192, 7168, 1, sm_count=152)
-    assert p["ctas"] == 304 and p["stages"] == 3 and p["threads"] == 32 + 224
-    # 12 and 16 inputs: one CTA per SM, 2 slots
-    for n in (12, 16):
-        p = arlib.ar_get_plan(n, 8192, 6144, 1, sm_count=152)
-        assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2
+    assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 3 and p["threads"] == 32 + 224
+    # 16 inputs: one CTA per SM, 2 slots
+    p = arlib.ar_get_plan(16, 8192, 6144, 1, sm_count=152)
+    assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2
     # 3 inputs: the register kernel
     assert arlib.ar_get_plan(3, 8192, 4096, 1, sm_count=152)["kernel"] == 1
+    # stage 2 of two-stage (one input) stays on the register kernel
+    assert arlib.ar_get_plan(8, 8192, 6144, 2, sm_count=152)["kernel"] == 1
     # H above the stream kernel's limit: the register kernel with a cluster
     p = arlib.ar_get_plan(3, 1000, 65536, 1, sm_count=152)
     assert p["kernel"] == 1 and p["cluster"] == 8
+    # rows of more than 1024 packs: stream for >= 5 inputs from 256 rows,
+    # for 4 inputs from max(4 x SMs, 1024) rows
+    assert arlib.ar_get_plan(8, 255, 16384, 1, sm_count=152)["kernel"] == 1
+    assert arlib.ar_get_plan(8, 256, 16384, 1, sm_count=152)["kernel"] == 2
+    assert arlib.ar_get_plan(4, 1023, 16384, 1, sm_count=152)["kernel"] == 1
+    assert arlib.ar_get_plan(4, 1024, 16384, 1, sm_count=152)["kernel"] == 2
+    assert arlib.ar_get_plan(4, 1215, 16384, 1, sm_count=304)["kernel"] == 1
+
+
+def plan_table():
+    """The launch plan's lookup table, parsed from its generated header:
+    (grid, SM count, score[inputs][packs][rows] = percentages per candidate)."""
+    text = open(os.path.join(ROOT, "allreduce_sum_residual_gb300", "csrc", "plan_table.cuh")).read()
+    grid = {name: [int(x) for x in re.search(name + r"\[\d+\] = \{([^}]*)\}", text).group(1).split(",")]
+            for name in ("kPlanInputs", "kPlanPacks", "kPlanRows")}
+    sms = int(re.search(r"kPlanTableSms = (\d+)", text).group(1))
+    body = text[text.index("kPlanScore["):]
+    cells = [[int(x) for x in c.split(",")] for c in re.findall(r"\{(\d+(?:,\d+){4})\}", body)]
+    ni, npk, nr = (len(grid[k]) for k in ("kPlanInputs", "kPlanPacks", "kPlanRows"))
+    assert len(cells) == ni * npk * nr
+    score = [[[cells[(i * npk + j) * nr + k] for k in range(nr)] for j in range(npk)] for i in range(ni)]
+    return grid, sms, score
+
+
+def _bracket(g, x):
+    if x <= g[0]:
+        return 0, 0
+    for i, v in enumerate(g):
+        if x == v:
+            return i, i
+        if x < v:
+            return i - 1, i
+    return len(g) - 1, len(g) - 1
+
+
+def _table_pick(grid, sms_table, score, n, m, P, sms):
+    """The lookup restated: bracketing inputs, packs and rows columns,
+    highest summed percentage (first on ties)."""
+    n0, n1 = _bracket(grid["kPlanInputs"], n)
+    p0, p1 = _bracket(grid["kPlanPacks"], P)
+    m0, m1 = _bracket(grid["kPlanRows"], m * sms_table / sms)
+    tot = [0] * 5
+    for i in range(n0, n1 + 1):
+        for j in range(p0, p1 + 1):
+            for k in range(m0, m1 + 1):
+                for c in range(5):
+                    tot[c] += score[i][j][k][c]
+    best = max(range(5), key=lambda c: (tot[c], -c))
+    return "S" if best == 0 else str(1 << (best - 1))
+
+
+def _expect(p, ch):
+    if ch == "S":
+        return p["kernel"] == 2
+    return p["kernel"] == 1 and p["cluster"] == 1 and p["vpt"] == int(ch)
+
+
+def test_plan_follows_the_measured_table_at_every_grid_point(arlib):
+    grid, sms, score = plan_table()
+    for i, n in enumerate(grid["kPlanInputs"]):
+        for j, P in enumerate(grid["kPlanPacks"]):
+            for k, m in enumerate(grid["kPlanRows"]):
+                s = score[i][j][k]
+                want = max(range(5), key=lambda c: (s[c], -c))
+                ch = "S" if want == 0 else str(1 << (want - 1))
+                p = arlib.ar_get_plan(n, m, 8 * P, 1, sm_count=sms)
+                assert _expect(p, ch), (n, P, m, ch, p)
+
+
+def test_plan_between_grid_points(arlib):
+    """Random shapes off the grid: the plan equals the restated lookup
+    (bracketing columns, SM scaling, shortest-column clamp, the one-input
+    row for stage 2 of two-stage)."""
+    import random
+    grid, sms, score = plan_table()
+    rng = random.Random(7)
+    for _ in range(3000):
+        n = rng.randint(1, 16)
+        H = 8 * rng.randint(4, grid["kPlanPacks"][-1])
+        m = int(round(10 ** rng.uniform(1.8, 4.6)))
+        sm = rng.choice((sms, sms // 2, 132, 160))
+        mode = rng.choice((1, 1, 1, 2))
+        p = arlib.ar_get_plan(n, m, H, mode, sm_count=sm)
+        inputs = n if mode == 1 else 1
+        if m < 64:
+            assert p["kernel"] == 1 and p["cluster"] >= 1
+            continue
+        ch = _table_pick(grid, sms, score, inputs, m, H // 8, sm)
+        assert _expect(p, ch), (n, m, H, mode, sm, ch, p)
 
 
 def test_plan_rejects_bad_shapes(arlib):
