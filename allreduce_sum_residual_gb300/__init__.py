@@ -11,6 +11,8 @@ Names follow the C ABI:
     ar_rmsnorm(partials, residual, weight, eps, out=None, residual_out=None,
                mode=AR_MODE_AUTO, stream=None) -> (out, residual_out)
     ar_rmsnorm_ex(..., sum_out=None, cluster=0, vpt=0)
+    ar_rmsnorm_mapped(partials, residual, weight, eps, out=None,
+                      residual_out=None, mode=AR_MODE_AUTO, stream=None, device=None)
     ar_reduce_scatter_flat(partials, temp, stream=None)
     ar_reduce_scatter_store(partials, temps, rank, stream=None)
     ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None)
@@ -72,6 +74,8 @@ _SIGS = {
     "ar_rmsnorm_ex": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP, ctypes.c_float,
                                      _I64, _I64, _VP, _VP, ctypes.c_int, _VP, _VP,
                                      ctypes.POINTER(ar_plan_t)]),
+    "ar_rmsnorm_mapped": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP,
+                                         ctypes.c_float, _I64, _I64, _VP, _VP, ctypes.c_int, _VP]),
     "ar_get_plan": (ctypes.c_int, [ctypes.c_int, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(ar_plan_t)]),
     "ar_reduce_scatter_flat": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _I64, _VP, _VP]),
@@ -180,6 +184,65 @@ def ar_rmsnorm(partials, residual, weight, eps, out=None, residual_out=None,
     st = lib().ar_rmsnorm(arr, len(partials), _ptr(residual), _ptr(weight), float(eps), m, H,
                           _ptr(out), _ptr(residual_out), int(mode), _stream_ptr(stream, dev))
     _check(st, "ar_rmsnorm")
+    return out, residual_out
+
+
+def _check_mapped_tensor(t, name, shape, device):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+    if t.is_cuda:
+        if t.device != device:
+            raise ValueError(f"{name} must be on {device} or in pinned host memory, got {t.device}")
+    elif t.numel() > 0 and not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or in pinned host memory")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def ar_rmsnorm_mapped(partials, residual, weight, eps, out=None, residual_out=None,
+                      mode=AR_MODE_AUTO, stream=None, device=None):
+    """ar_rmsnorm where any tensor may be in pinned host memory (CPU tensors
+    with ``is_pinned()``): the kernels on ``device`` (default: the CUDA
+    tensors' device, else the current device) read and write those buffers
+    over the host link.  Missing outputs are allocated pinned on the host
+    when the residual is on the host, else on its device.  Asynchronous on
+    the stream: host outputs are valid once the stream has passed the call.
+    Returns (out, residual_out)."""
+    import torch
+    mode = MODES.get(mode, mode)
+    if len(partials) < 1:
+        raise ValueError("need at least one partial")
+    if residual.dim() != 2:
+        raise ValueError("residual must be [m, H]")
+    m, H = residual.shape
+    tensors = list(partials) + [residual, weight] + [t for t in (out, residual_out) if t is not None]
+    if device is None:
+        cuda = [t.device for t in tensors if isinstance(t, torch.Tensor) and t.is_cuda]
+        device = cuda[0] if cuda else torch.device("cuda", torch.cuda.current_device())
+    device = torch.device(device)
+    for k, p in enumerate(partials):
+        _check_mapped_tensor(p, f"partials[{k}]", (m, H), device)
+    _check_mapped_tensor(residual, "residual", (m, H), device)
+    _check_mapped_tensor(weight, "weight", (H,), device)
+    if out is None:
+        out = torch.empty((m, H), dtype=torch.bfloat16, device=residual.device,
+                          pin_memory=not residual.is_cuda)
+    if residual_out is None:
+        residual_out = torch.empty((m, H), dtype=torch.bfloat16, device=residual.device,
+                                   pin_memory=not residual.is_cuda)
+    _check_mapped_tensor(out, "out", (m, H), device)
+    _check_mapped_tensor(residual_out, "residual_out", (m, H), device)
+    arr = (_VP * len(partials))(*[p.data_ptr() for p in partials])
+    with torch.cuda.device(device):
+        st = lib().ar_rmsnorm_mapped(arr, len(partials), _ptr(residual), _ptr(weight), float(eps),
+                                     m, H, _ptr(out), _ptr(residual_out), int(mode),
+                                     _stream_ptr(stream, device))
+    _check(st, "ar_rmsnorm_mapped")
     return out, residual_out
 
 

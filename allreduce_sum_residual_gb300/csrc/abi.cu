@@ -512,9 +512,47 @@ static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n
   a->status = status;
 }
 
+// True if the current device `dev` can use `p` at the same address: its own
+// device memory, managed memory, or host memory that is pinned and mapped
+// (cudaHostAlloc, cudaHostRegister; with unified addressing the device
+// address equals the host address).  Pageable host memory, another device's
+// memory and unknown pointers are refused.
+static bool device_accessible(const void *p, int dev) {
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == dev;
+    case cudaMemoryTypeManaged: return true;
+    case cudaMemoryTypeHost: return at.devicePointer == p;
+    default: return false;
+  }
+}
+
+static int check_mapped(const void *const *partials, int n, const void *residual,
+                        const void *weight, const void *out, const void *residual_out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  for (int k = 0; k < n; ++k)
+    if (!device_accessible(partials[k], dev)) return AR_ERR_ARG;
+  if (!device_accessible(residual, dev) || !device_accessible(weight, dev) ||
+      !device_accessible(out, dev) || !device_accessible(residual_out, dev))
+    return AR_ERR_ARG;
+  return AR_OK;
+}
+
+// `mapped`: any buffer may be pinned host memory (checked per pointer); the
+// epilogue then runs on the register kernel, whose plain loads and stores
+// reach host memory over the host link.  (The stream kernel's bulk copies
+// are kept to device memory.)
 static int run(const void *const *partials, int n, const void *residual, const void *weight,
                float eps, int64_t m, int64_t H, void *out, void *residual_out, int mode,
-               void *stream, float *sum_out, const ar_plan_t *force) {
+               void *stream, float *sum_out, const ar_plan_t *force, bool mapped = false) {
   int st = check_shape(n, m, H, eps);
   if (st != AR_OK) return st;
   if (mode != AR_MODE_AUTO && mode != AR_MODE_ONE_STAGE && mode != AR_MODE_TWO_STAGE)
@@ -522,6 +560,14 @@ static int run(const void *const *partials, int n, const void *residual, const v
   if (m == 0) return AR_OK;  // nothing is read or written; pointers may be null
   st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, sum_out);
   if (st != AR_OK) return st;
+  ar_plan_t register_only;
+  if (mapped) {
+    st = check_mapped(partials, n, residual, weight, out, residual_out);
+    if (st != AR_OK) return st;
+    std::memset(&register_only, 0, sizeof register_only);
+    register_only.kernel = AR_KERNEL_REGISTER;
+    force = &register_only;
+  }
   DeviceState *d = current_device(&st);
   if (!d) return st;
   ar_plan_t pl;
@@ -635,6 +681,13 @@ int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual, cons
                   void *stream, float *sum_out, const ar_plan_t *plan) {
   return run(partials, n, residual, weight, eps, m, H, out, residual_out, mode, stream, sum_out,
              plan);
+}
+
+int ar_rmsnorm_mapped(const void *const *partials, int n, const void *residual,
+                      const void *weight, float eps, int64_t m, int64_t H, void *out,
+                      void *residual_out, int mode, void *stream) {
+  return run(partials, n, residual, weight, eps, m, H, out, residual_out, mode, stream, nullptr,
+             nullptr, true);
 }
 
 int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count, ar_plan_t *plan) {

@@ -163,6 +163,29 @@ int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
                   float *sum_out, const ar_plan_t *plan);
 
 /*
+ * As ar_rmsnorm, but any of the partials, residual, weight, out and
+ * residual_out may live in host memory that is pinned and mapped into the
+ * device's address space (cudaHostAlloc / cudaMallocHost, or
+ * cudaHostRegister, under unified addressing: the device address equals the
+ * host address).  The kernels read and write such buffers directly over the
+ * host link (NVLink-C2C on Grace systems): no staging copy, no device memory
+ * beyond the two-stage workspace.  The epilogue runs on the register kernel
+ * (plain 16-byte loads and stores).  Results are bit-identical to
+ * ar_rmsnorm's register kernel for the same launch shape.
+ *
+ * Each pointer is checked with cudaPointerGetAttributes before anything is
+ * launched: it must be device memory of the current device, managed
+ * memory, or mapped pinned host memory; anything else (pageable host
+ * memory, another device's memory) returns AR_ERR_ARG.  As everywhere in
+ * this library, each buffer must hold the bytes its shape implies.  The
+ * host memory must stay pinned and untouched by the host until the stream
+ * has passed the call.  The checks cost a few microseconds per call.
+ */
+int ar_rmsnorm_mapped(const void *const *partials, int n, const void *residual,
+                      const void *weight, float eps, int64_t m, int64_t H,
+                      void *out, void *residual_out, int mode, void *stream);
+
+/*
  * Stage 1 alone: temp[e] = bf16(p_0[e] + ... + p_{n-1}[e]) for e < count,
  * fp32 rank-order sum, one 16-byte pack per thread step, no shared memory
  * and no block barrier (ROCm/aiter #3817, Technical Details, 2stage,

@@ -24,7 +24,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     names = declared_functions()
-    for must in ("ar_rmsnorm", "ar_rmsnorm_ex", "ar_reduce_scatter_flat", "ar_load_rmsnorm",
+    for must in ("ar_rmsnorm", "ar_rmsnorm_ex", "ar_rmsnorm_mapped", "ar_reduce_scatter_flat",
+                 "ar_load_rmsnorm",
                  "ar_reserve_workspace", "ar_release_workspace", "ar_select_mode",
                  "ar_get_plan", "ar_strerror"):
         assert must in names
@@ -118,6 +119,24 @@ def test_stage_entry_points_check_arguments(arlib):
                              BASE + 16384, None) == OK
     assert L.ar_load_rmsnorm(BASE, BASE + 4096, BASE + 8192, -1.0, 1, 1024, BASE + 12288,
                              BASE + 16384, None) == ARG
+
+
+def test_mapped_entry_point_checks_arguments_before_touching_memory(arlib):
+    """ar_rmsnorm_mapped runs the same shape, alignment and alias checks as
+    ar_rmsnorm before its per-pointer memory-type checks; on a machine
+    without a GPU those report AR_ERR_CUDA, never a launch."""
+    L = arlib.lib()
+    arr = (ctypes.c_void_p * 2)(BASE, BASE + (1 << 20))
+    f = ctypes.c_float
+    call = lambda n, m, H, out, rout, eps=1e-6: L.ar_rmsnorm_mapped(
+        arr, n, BASE + (2 << 20), BASE + (3 << 20), f(eps), m, H, out, rout, 1, None)
+    assert call(0, 4, 1024, BASE + (4 << 20), BASE + (5 << 20)) == ARG
+    assert call(2, 4, 1020, BASE + (4 << 20), BASE + (5 << 20)) == ALIGN
+    assert call(2, 4, 1024, BASE + (4 << 20), BASE + (5 << 20), eps=-1.0) == ARG
+    assert call(2, 4, 1024, BASE, BASE + (5 << 20)) == ALIAS
+    assert call(2, 0, 1024, None, None) == OK
+    assert call(2, 4, 1024, BASE + (4 << 20) + 8, BASE + (5 << 20)) == ALIGN
+    assert call(2, 4, 1024, BASE + (4 << 20), BASE + (5 << 20)) == arlib.AR_ERR_CUDA
 
 
 def test_select_mode_is_host_logic(arlib):

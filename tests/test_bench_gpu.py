@@ -34,6 +34,8 @@ def test_bench_prints_the_contract_line(arlib):
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["residual_out_equals_device_path"] is True
+    assert e["copy_engines"]["value"] > 0
     assert d["gpu_launches"] == steps * d["config"]["plan"]["launches"]
     assert set(d["clocks"]) >= {"sm_mhz", "sm_max_mhz", "reasons"}
     # value is bytes per step x steps over the timed region, in GB/s
