@@ -194,6 +194,18 @@ def sum_over_ranks(world, x, device=None):
 
 # ---------------------------------------------------------------- our arm
 
+def settle(device=None):
+    """Wait for all work queued so far (on every stream) before side-stream
+    work starts.  Inputs and outputs are made on the default stream; a
+    kernel launched on a side stream is not ordered after that work, and the
+    caching allocator may hand it memory a default-stream kernel is still
+    reading (a temporary of the input generator), which would corrupt the
+    inputs.  Every function here that launches on a side stream settles
+    first."""
+    import torch
+    torch.cuda.synchronize(device)
+
+
 def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=100):
     """W warm-up steps, then exactly K steps timed with CUDA events on
     `stream`, bracketed by barrier + synchronize.  With `use_graph` the K
@@ -201,6 +213,7 @@ def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=
     the remainder), so host launch overhead stays out of the timed region,
     as in the pages' method.  Returns (total_s, mean step s)."""
     import torch
+    settle(device)
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(device)
@@ -254,6 +267,7 @@ def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=No
             arn.ar_rmsnorm_ex(i.partials, i.residual, i.weight, eps, out=o, residual_out=r,
                               mode=mode, kernel=shape[0], cluster=shape[1], vpt=shape[2], **extra)
 
+    settle()
     with torch.cuda.stream(stream):
         for i, (o, r) in zip(inps, outs):
             call(i, o, r)
@@ -317,6 +331,7 @@ def unfused_torch_us(inp, stream, calls=50, replays=5):
         out = torch.nn.functional.rms_norm(r, (H,), w, eps=inp.eps).to(torch.bfloat16)
         return out, rout
 
+    settle()
     with torch.cuda.stream(stream):
         call()
     torch.cuda.synchronize()
@@ -356,6 +371,7 @@ def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
             arn.ar_reduce_scatter_store(inp.partials, temps, r)
         arn.ar_load_rmsnorm(temps[0], inp.residual, inp.weight, inp.eps, out=out, residual_out=rout)
 
+    settle()
     with torch.cuda.stream(stream):
         call()
     torch.cuda.synchronize()
@@ -383,6 +399,7 @@ def empty_node_floor_us(stream, calls=2000, replays=20):
     fill): the launch-and-complete floor any dependent kernel chain pays."""
     import torch
     x = torch.zeros(1, device="cuda")
+    settle()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for _ in range(calls):
@@ -455,6 +472,7 @@ def e2e_measure(arn, inp, mode, stream, steps):
             ho.copy_(do, non_blocking=True)
             hro.copy_(dro, non_blocking=True)
 
+    settle()
     step()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
@@ -489,6 +507,7 @@ def e2e_mapped(arn, inp, mode, stream, steps):
         arn.ar_rmsnorm_mapped(hp, hr, hw, inp.eps, out=ho, residual_out=hro, mode=mode,
                               stream=stream, device=inp.residual.device)
 
+    settle()
     step()
     torch.cuda.synchronize()
     # the outputs of the device path, for a check that the host path wrote them
@@ -574,6 +593,7 @@ def e2e_pipelined(arn, inp, mode, steps, chunks=8):
             best = min(best, a.elapsed_time(b) / 1e3)
         return best
 
+    settle()
     step()
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)

@@ -349,6 +349,7 @@ def test_graph_capture_and_replay():
     s = torch.cuda.Stream()
     out = torch.empty_like(inp.residual)
     rout = torch.empty_like(inp.residual)
+    s.wait_stream(torch.cuda.current_stream())  # the inputs were made on the default stream
     with torch.cuda.stream(s):
         arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, out=out, residual_out=rout,
                        mode="two_stage")
