@@ -55,7 +55,9 @@ class ArError(RuntimeError):
 AR_KERNEL_AUTO = 0
 AR_KERNEL_REGISTER = 1
 AR_KERNEL_STREAM = 2
-KERNELS = {"auto": AR_KERNEL_AUTO, "register": AR_KERNEL_REGISTER, "stream": AR_KERNEL_STREAM}
+AR_KERNEL_REGISTER_LATE_W = 3
+KERNELS = {"auto": AR_KERNEL_AUTO, "register": AR_KERNEL_REGISTER, "stream": AR_KERNEL_STREAM,
+           "register_late": AR_KERNEL_REGISTER_LATE_W}
 
 
 class ar_plan_t(ctypes.Structure):
@@ -250,7 +252,7 @@ def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
                   mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0, kernel=0,
                   threads=0, stages=0, ctas=0):
     """ar_rmsnorm plus the reduced sum (fp32 [m, H] ``sum_out``) and a forced
-    kernel ("register" / "stream") and launch shape: register kernel
+    kernel ("register" / "register_late" / "stream") and launch shape: register kernel
     ``cluster`` CTAs per row and ``vpt`` packs per thread; stream kernel
     ``threads`` (32 + consumers), ring ``stages`` and grid ``ctas``.  0 =
     library's choice.  Returns (out, residual_out, sum_out)."""

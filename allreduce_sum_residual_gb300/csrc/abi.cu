@@ -24,6 +24,10 @@ EpilogueKernel epilogue_cluster_kernel_group0(int n, int vpt_log2);
 EpilogueKernel epilogue_cluster_kernel_group1(int n, int vpt_log2);
 EpilogueKernel epilogue_cluster_kernel_group2(int n, int vpt_log2);
 EpilogueKernel epilogue_cluster_kernel_group3(int n, int vpt_log2);
+EpilogueKernel epilogue_late_kernel_group0(int n, int vpt_log2);
+EpilogueKernel epilogue_late_kernel_group1(int n, int vpt_log2);
+EpilogueKernel epilogue_late_kernel_group2(int n, int vpt_log2);
+EpilogueKernel epilogue_late_kernel_group3(int n, int vpt_log2);
 cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream);
 StreamKernel stream_kernel_group0(int n, int vpt_log2);
 StreamKernel stream_kernel_group1(int n, int vpt_log2);
@@ -36,9 +40,16 @@ constexpr int kAssumedSmemOptin = 232448;         // sm_100-class opt-in per CTA
 
 static int vpt_log2(int vpt) { return vpt == 1 ? 0 : vpt == 2 ? 1 : vpt == 4 ? 2 : vpt == 8 ? 3 : -1; }
 
-EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered) {
+EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered, bool late_weight) {
   const int l = vpt_log2(vpt);
   if (n < 1 || n > AR_MAX_RANKS || l < 0) return nullptr;
+  if (clustered && late_weight) return nullptr;
+  if (late_weight) switch ((n - 1) / 4) {
+      case 0: return epilogue_late_kernel_group0(n, l);
+      case 1: return epilogue_late_kernel_group1(n, l);
+      case 2: return epilogue_late_kernel_group2(n, l);
+      default: return epilogue_late_kernel_group3(n, l);
+    }
   if (clustered) switch ((n - 1) / 4) {
       case 0: return epilogue_cluster_kernel_group0(n, l);
       case 1: return epilogue_cluster_kernel_group1(n, l);
@@ -113,7 +124,7 @@ static DeviceState *current_device(int *status) {
     // Rows split over up to 16 CTAs need the non-portable cluster size.
     for (int n = 1; n <= AR_MAX_RANKS; ++n)
       for (int vpt = 1; vpt <= 8; vpt *= 2) {
-        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(epilogue_kernel(n, vpt, true)),
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(epilogue_kernel(n, vpt, true, false)),
                                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
           cudaGetLastError();
           *status = AR_ERR_CUDA;
@@ -216,10 +227,10 @@ static int select_mode(int n, int64_t m, int64_t H) {
 // axis where it falls between two: inputs, packs, rows) are added up and
 // the best sum wins, which prefers a candidate that is good on both sides
 // of a cliff.  Rows are first scaled to the table's SM count; rows
-// shorter than the table's shortest use its column.  Returns 0 for the
-// stream kernel, the register kernel's packs per thread, or -1 where the
-// table does not apply (fewer than 64 rows, where the register kernel
-// spreads a row over a cluster, or rows longer than the table's longest).
+// shorter than the table's shortest use its column.  Returns the kernel
+// and its packs per thread, or kernel 0 where the table does not apply
+// (fewer than 64 rows, where the register kernel spreads a row over a
+// cluster, or rows longer than the table's longest).
 constexpr int64_t kTableMinRows = 64;
 
 // The grid columns around x: [lo, hi] = [i - 1, i] between two columns,
@@ -249,8 +260,22 @@ static int last_of(const int (&grid)[K]) {
   return grid[K - 1];
 }
 
-static int table_choice(int inputs, int64_t m, int64_t P, int sms) {
-  if (m < kTableMinRows || P > last_of(kPlanPacks)) return -1;
+struct TableChoice {
+  int kernel;  // AR_KERNEL_STREAM, AR_KERNEL_REGISTER or AR_KERNEL_REGISTER_LATE_W; 0: no table
+  int vpt;     // register kernels: packs per thread
+};
+
+// Candidate c of the table: 0 the stream kernel; 1 .. 4 the register
+// kernel with 1, 2, 4, 8 packs per thread; 5 .. 8 the same with the weight
+// loaded after the sums.
+static TableChoice candidate(int c) {
+  if (c == 0) return {AR_KERNEL_STREAM, 0};
+  if (c <= 4) return {AR_KERNEL_REGISTER, 1 << (c - 1)};
+  return {AR_KERNEL_REGISTER_LATE_W, 1 << (c - 5)};
+}
+
+static TableChoice table_choice(int inputs, int64_t m, int64_t P, int sms) {
+  if (m < kTableMinRows || P > last_of(kPlanPacks)) return {0, 0};
   int n0, n1, p0, p1, m0, m1;
   bracket(kPlanInputs, static_cast<double>(inputs), &n0, &n1);
   bracket(kPlanPacks, static_cast<double>(P), &p0, &p1);
@@ -263,7 +288,7 @@ static int table_choice(int inputs, int64_t m, int64_t P, int sms) {
   int best = 0;
   for (int c = 1; c < kPlanCandidates; ++c)
     if (score[c] > score[best]) best = c;
-  return best == 0 ? 0 : 1 << (best - 1);
+  return candidate(best);
 }
 
 // Rows of more than 1024 packs (beyond the table): the stream kernel for 4
@@ -393,8 +418,10 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
     fk = force->kernel;
     fc = force->cluster;
     fv = force->vpt;
-    if (fk != AR_KERNEL_AUTO && fk != AR_KERNEL_REGISTER && fk != AR_KERNEL_STREAM)
+    if (fk != AR_KERNEL_AUTO && fk != AR_KERNEL_REGISTER && fk != AR_KERNEL_STREAM &&
+        fk != AR_KERNEL_REGISTER_LATE_W)
       return AR_ERR_ARG;
+    if (fk == AR_KERNEL_REGISTER_LATE_W && fc > 1) return AR_ERR_ARG;
     if (fc != 0 && fc != 1 && fc != 2 && fc != 4 && fc != 8 && fc != 16) return AR_ERR_ARG;
     if (fv != 0 && vpt_log2(fv) < 0) return AR_ERR_ARG;
     if (fk == AR_KERNEL_STREAM && (fc > 1 || fv != 0)) return AR_ERR_ARG;
@@ -406,14 +433,22 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
   const bool shape_forced = fc != 0 || fv != 0;
-  const int choice = table_choice(inputs, m, P, sms);
+  const TableChoice choice = table_choice(inputs, m, P, sms);
   bool want_stream = fk == AR_KERNEL_STREAM;
   if (fk == AR_KERNEL_AUTO && !shape_forced)
-    want_stream = choice >= 0 ? choice == 0 : long_rows_want_stream(inputs, m, sms);
+    want_stream = choice.kernel ? choice.kernel == AR_KERNEL_STREAM
+                                : long_rows_want_stream(inputs, m, sms);
   if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin,
                                    fk == AR_KERNEL_STREAM ? force : nullptr, pl))) {
     if (fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
-    plan_register(m, P, inputs, fc, fv, choice > 0 ? choice : 0, pl);
+    const bool table_register = choice.kernel == AR_KERNEL_REGISTER ||
+                                choice.kernel == AR_KERNEL_REGISTER_LATE_W;
+    plan_register(m, P, inputs, fc, fv, table_register ? choice.vpt : 0, pl);
+    const bool late = fk == AR_KERNEL_REGISTER_LATE_W ||
+                      (fk == AR_KERNEL_AUTO && !shape_forced &&
+                       choice.kernel == AR_KERNEL_REGISTER_LATE_W);
+    if (late && pl->cluster == 1) pl->kernel = AR_KERNEL_REGISTER_LATE_W;
+    if (fk == AR_KERNEL_REGISTER_LATE_W && pl->cluster != 1) return AR_ERR_ARG;
     const int64_t per_cta = (P + pl->cluster - 1) / pl->cluster;
     if (per_cta > kMaxPacksPerCta) return AR_ERR_ARG;  // forced shape too small
   }
@@ -450,7 +485,8 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
   cfg.numAttrs = na;
   EpilogueArgs args = a;
   args.early_reads = after_prior ? 1 : 0;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, epilogue_kernel(n, pl.vpt, pl.cluster > 1), args);
+  const cudaError_t e = cudaLaunchKernelEx(
+      &cfg, epilogue_kernel(n, pl.vpt, pl.cluster > 1, pl.kernel == AR_KERNEL_REGISTER_LATE_W), args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -50,9 +50,16 @@ __device__ __forceinline__ void sum_pack_in_rank_order(const uint4 *const (&p)[A
 // per-row launch uses the CL = false instantiation, which has no exchange
 // code and so keeps the register count (and the CTAs per SM) of a plain
 // row kernel.
-template <int N, int VPT, bool CL>
+// LW (one CTA per row only): load the weight after the sums instead of
+// with the inputs.  Its registers are then free while the n partials are
+// in flight -- 3 to 11 fewer a thread for n = 4 .. 8 at one pack per
+// thread, enough for a second CTA per SM at some row lengths -- at the
+// price of one more (L2-resident) load before the output.  The launch plan
+// picks whichever is faster for the shape.
+template <int N, int VPT, bool CL, bool LW = false>
 __global__ void __launch_bounds__(1024 / VPT)
 k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
+  static_assert(!(CL && LW), "the late weight load is for one CTA per row");
   __shared__ float red[33];
   __shared__ float cta_totals[kMaxClusterCtas];
   __shared__ uint64_t totals_bar;  // completes when the S cluster totals have arrived
@@ -86,7 +93,7 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
     if (c < c1) {
-      wv[v] = ld_ro(a.w + c);
+      if constexpr (!LW) wv[v] = ld_ro(a.w + c);
       rv[v] = ld_ro(a.res + base + c);
     }
   }
@@ -122,6 +129,13 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
     for (int e = 0; e < 8; ++e) ss = fmaf(r[v][e], r[v][e], ss);
   }
 
+  if constexpr (LW) {
+#pragma unroll
+    for (int v = 0; v < VPT; ++v) {
+      const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
+      if (c < c1) wv[v] = ld_ro(a.w + c);
+    }
+  }
   float total = block_sum(ss, red);
   if constexpr (CL) {
     cluster_wait_acquire();  // every peer runs and has initialised its barrier
@@ -146,9 +160,9 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   }
 }
 
-// Kernel pointer for (n, vpt, clustered); n in [1, AR_MAX_RANKS], vpt in
-// {1, 2, 4, 8}.
+// Kernel pointer for (n, vpt, clustered, late weight); n in [1,
+// AR_MAX_RANKS], vpt in {1, 2, 4, 8}; late weight only without a cluster.
 using EpilogueKernel = void (*)(EpilogueArgs);
-EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered);
+EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered, bool late_weight);
 
 }  // namespace arn

@@ -902,6 +902,12 @@ def run_shapes(args):
         torch.cuda.empty_cache()
 
 
+# bench.py --kernels candidates: name -> forced (kernel, cluster, vpt)
+KERNEL_CANDIDATES = {"stream": ("stream", 0, 0),
+                     **{f"register{v}": ("register", 0, v) for v in (1, 2, 4, 8)},
+                     **{f"late{v}": ("register_late", 0, v) for v in (1, 2, 4, 8)}}
+
+
 def run_kernels(args):
     """Register vs stream kernel for one-stage at many rows, over n and H
     (graph method, cold sets); one JSON line per case."""
@@ -923,9 +929,8 @@ def run_kernels(args):
                 base = synth.make_inputs(w, m, backend="torch", device="cuda")
                 inps = cold_sets(synth, w, m, base, l2, calls)
                 row = {"n": n, "H": H, "m": m, "bytes": set_bytes}
-                for shape in (None, ("stream", 0, 0), ("register", 0, 1), ("register", 0, 2),
-                              ("register", 0, 4), ("register", 0, 8)):
-                    key = "auto" if shape is None else f"{shape[0]}{shape[2] or ''}"
+                shapes = [None] + [KERNEL_CANDIDATES[c] for c in args.kernel_cands.split(",")]
+                for key, shape in zip(["auto"] + args.kernel_cands.split(","), shapes):
                     try:
                         t = graph_latency(arn, inps, "one_stage", w.eps, stream, calls, replays, shape)
                         row[key] = round(set_bytes / t / 1e9, 1)
@@ -980,11 +985,13 @@ def main(argv=None):
     ap.add_argument("--kernel-ns", default="1,2,3,4,8,16", help="--kernels: input counts")
     ap.add_argument("--kernel-hs", default="4096,7168", help="--kernels: hidden sizes")
     ap.add_argument("--kernel-ms", default="304,1024,4096,16384", help="--kernels: token counts")
+    ap.add_argument("--kernel-cands", default=",".join(KERNEL_CANDIDATES),
+                    help="--kernels: candidates (stream, register1..8, late1..8)")
     ap.add_argument("--quick", action="store_true", help="shorter latency table and baselines")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
     ap.add_argument("--mode", default="auto", choices=("auto", "one_stage", "two_stage"))
-    ap.add_argument("--kernel", default="auto", choices=("auto", "register", "stream"),
+    ap.add_argument("--kernel", default="auto", choices=("auto", "register", "register_late", "stream"),
                     help="force the epilogue kernel (profiling)")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one from Python instead of from graphs")

@@ -112,7 +112,8 @@ int ar_rmsnorm(const void *const *partials, int n, const void *residual,
  */
 typedef struct {
   int mode;        /* AR_MODE_ONE_STAGE or AR_MODE_TWO_STAGE                  */
-  int kernel;      /* AR_KERNEL_REGISTER or AR_KERNEL_STREAM                   */
+  int kernel;      /* AR_KERNEL_REGISTER, AR_KERNEL_REGISTER_LATE_W or
+                      AR_KERNEL_STREAM                                        */
   int cluster;     /* register kernel: CTAs sharing one row, 1..16            */
   int vpt;         /* 16-byte packs per thread: 1, 2, 4 or 8 (stream kernel:
                       row tiles per row, rounded up to a power of two)       */
@@ -129,6 +130,10 @@ typedef struct {
 #define AR_KERNEL_STREAM    2  /* persistent, one CTA per SM; a producer warp
                                   streams row tiles into a shared-memory ring
                                   with bulk asynchronous copies: many rows   */
+#define AR_KERNEL_REGISTER_LATE_W 3  /* the register kernel, one CTA per row,
+                                        loading the weight after the sums:
+                                        fewer registers while the partials
+                                        are in flight (more CTAs per SM)  */
 
 /*
  * The plan ar_rmsnorm would follow for (n, m, H, mode) on a GPU with
@@ -147,8 +152,9 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count,
  *            skip.  Costs 4*m*H extra bytes of writes.
  *   plan     NULL for the library's choice, else it forces the epilogue
  *            kernel and its launch shape; 0 in a field = library's choice.
- *            `kernel`: AR_KERNEL_REGISTER or AR_KERNEL_STREAM.  Register
- *            kernel: `cluster` in {1,2,4,8,16}, `vpt` in {1,2,4,8}, at most
+ *            `kernel`: AR_KERNEL_REGISTER, AR_KERNEL_REGISTER_LATE_W or
+ *            AR_KERNEL_STREAM.  Register kernel: `cluster` in {1,2,4,8,16}
+ *            (1 for AR_KERNEL_REGISTER_LATE_W), `vpt` in {1,2,4,8}, at most
  *            1024 packs per CTA.  Stream kernel (H <= 32768): `threads` =
  *            32 + consumer threads (a multiple of 32, consumers <= 512, a row
  *            in <= 8 tiles), `stages` <= 16 ring slots (fewer if shared

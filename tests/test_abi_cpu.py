@@ -160,7 +160,7 @@ def test_plan_covers_every_pack(arlib, n, m, H, mode):
     assert p["mode"] in (1, 2) and (mode == 0 or p["mode"] == mode)
     assert p["launches"] == (2 if p["mode"] == 2 else 1)
     assert p["vpt"] in (1, 2, 4, 8)
-    if p["kernel"] == 1:   # register kernel: one CTA or a cluster per row
+    if p["kernel"] in (1, 3):   # register kernel: one CTA or a cluster per row
         per_cta = -(-P // p["cluster"])
         assert p["cluster"] in (1, 2, 4, 8, 16) and p["stages"] == 0
         assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024 // p["vpt"]
@@ -189,9 +189,10 @@ def test_plan_spreads_small_batches(arlib):
     # each with a 2-slot ring of 9 x 4 KB tiles (144 KB in flight per SM)
     p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 2 and p["threads"] == 288
-    # 4 inputs, H = 7168: two CTAs per SM with 3 slots of 5 x 3.5 KB
+    # 4 inputs, H = 7168, many rows: the register kernel with the weight
+    # loaded after the sums, one pack per thread (two 896-thread CTAs per SM)
     p = arlib.ar_get_plan(4, 8192, 7168, 1, sm_count=152)
-    assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 3 and p["threads"] == 32 + 224
+    assert p["kernel"] == 3 and p["vpt"] == 1 and p["threads"] == 896 and p["cluster"] == 1
     # 16 inputs: one CTA per SM, 2 slots
     p = arlib.ar_get_plan(16, 8192, 6144, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2
@@ -219,7 +220,9 @@ def plan_table():
             for name in ("kPlanInputs", "kPlanPacks", "kPlanRows")}
     sms = int(re.search(r"kPlanTableSms = (\d+)", text).group(1))
     body = text[text.index("kPlanScore["):]
-    cells = [[int(x) for x in c.split(",")] for c in re.findall(r"\{(\d+(?:,\d+){4})\}", body)]
+    ncand = int(re.search(r"kPlanCandidates = (\d+)", text).group(1))
+    cells = [[int(x) for x in c.split(",")]
+             for c in re.findall(r"\{(\d+(?:,\d+){%d})\}" % (ncand - 1), body)]
     ni, npk, nr = (len(grid[k]) for k in ("kPlanInputs", "kPlanPacks", "kPlanRows"))
     assert len(cells) == ni * npk * nr
     score = [[[cells[(i * npk + j) * nr + k] for k in range(nr)] for j in range(npk)] for i in range(ni)]
@@ -243,19 +246,26 @@ def _table_pick(grid, sms_table, score, n, m, P, sms):
     n0, n1 = _bracket(grid["kPlanInputs"], n)
     p0, p1 = _bracket(grid["kPlanPacks"], P)
     m0, m1 = _bracket(grid["kPlanRows"], m * sms_table / sms)
-    tot = [0] * 5
+    nc = len(score[0][0][0])
+    tot = [0] * nc
     for i in range(n0, n1 + 1):
         for j in range(p0, p1 + 1):
             for k in range(m0, m1 + 1):
-                for c in range(5):
+                for c in range(nc):
                     tot[c] += score[i][j][k][c]
-    best = max(range(5), key=lambda c: (tot[c], -c))
-    return "S" if best == 0 else str(1 << (best - 1))
+    return _cand_char(max(range(nc), key=lambda c: (tot[c], -c)))
+
+
+def _cand_char(c):
+    """Candidate index -> the header's winner character."""
+    return "S1248abcd"[c]
 
 
 def _expect(p, ch):
     if ch == "S":
         return p["kernel"] == 2
+    if ch in "abcd":
+        return p["kernel"] == 3 and p["cluster"] == 1 and p["vpt"] == 1 << "abcd".index(ch)
     return p["kernel"] == 1 and p["cluster"] == 1 and p["vpt"] == int(ch)
 
 
@@ -265,8 +275,7 @@ def test_plan_follows_the_measured_table_at_every_grid_point(arlib):
         for j, P in enumerate(grid["kPlanPacks"]):
             for k, m in enumerate(grid["kPlanRows"]):
                 s = score[i][j][k]
-                want = max(range(5), key=lambda c: (s[c], -c))
-                ch = "S" if want == 0 else str(1 << (want - 1))
+                ch = _cand_char(max(range(len(s)), key=lambda c: (s[c], -c)))
                 p = arlib.ar_get_plan(n, m, 8 * P, 1, sm_count=sms)
                 assert _expect(p, ch), (n, P, m, ch, p)
 

@@ -49,7 +49,7 @@ def test_host_buffers_match_oracle_and_device_path(n, m, H, mode):
     compare((out, rout, None), orc, f"mapped n={n} m={m} H={H} {mode}")
     # the same register-kernel shape on device memory gives the same bits
     plan = arn.ar_get_plan(n, m, H, {"one_stage": 1, "two_stage": 2, "auto": 0}[mode])
-    if plan["kernel"] == arn.AR_KERNEL_REGISTER:
+    if plan["kernel"] in (arn.AR_KERNEL_REGISTER, arn.AR_KERNEL_REGISTER_LATE_W):
         d_out, d_rout, _ = arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, inp.eps,
                                              mode=mode, cluster=plan["cluster"], vpt=plan["vpt"],
                                              kernel="register")

@@ -151,6 +151,32 @@ def test_launch_shape_does_not_change_results(cluster, vpt):
     check_full(inp, "one_stage", f"cluster={cluster} vpt={vpt}", cluster=cluster, vpt=vpt)
 
 
+@pytest.mark.parametrize("n,m,H,vpt", [(1, 300, 2056, 1), (4, 257, 7168, 1), (5, 64, 6144, 2),
+                                       (8, 100, 4104, 4), (3, 7, 1024, 8), (16, 130, 8192, 2),
+                                       (6, 1000, 8, 1)])
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_late_weight_register_kernel(n, m, H, vpt, mode):
+    """The register kernel that loads the weight after the sums: against the
+    oracle, and bit for bit against the same shape with the weight loaded
+    up front (only the load order differs)."""
+    w = synth.Workload("late", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m, seed=3)
+    late = run_gpu(inp, mode, cluster=1, vpt=vpt, kernel="register_late")
+    early = run_gpu(inp, mode, cluster=1, vpt=vpt, kernel="register")
+    torch.cuda.synchronize()
+    for a, b in zip(late, early):
+        assert torch.equal(a.view(torch.int16 if a.dtype == torch.bfloat16 else torch.int32),
+                           b.view(torch.int16 if b.dtype == torch.bfloat16 else torch.int32))
+    orc = oracle_rows(inp, None, mode == "two_stage")
+    compare(late, orc, f"late weight n={n} m={m} H={H} vpt={vpt} {mode}")
+
+
+def test_late_weight_needs_one_cta_per_row():
+    inp = device_inputs(synth.Workload("late2", n=2, H=1024, ms=(4,), p_std=0.5, res_std=1.0), 4)
+    with pytest.raises(arn.ArError):
+        run_gpu(inp, "one_stage", cluster=2, vpt=1, kernel="register_late")
+
+
 @pytest.mark.parametrize("m,H", [(1, 8), (3, 24), (2, 1032), (5, 7176), (153, 4104), (1, 131072),
                                  (2, 65544), (300, 8)])
 @pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
@@ -372,9 +398,13 @@ def test_stream_kernel_in_a_graph_matches_eager(mode):
     gives the same bits as the same call launched eagerly."""
     w = synth.Workload("graph", n=8, H=6144, ms=(1536,), p_std=0.5, res_std=1.0)
     inp = device_inputs(w, 1536)
-    if mode == "one_stage":
-        assert arn.ar_get_plan(8, 1536, 6144, 1)["kernel"] == arn.AR_KERNEL_STREAM
-    ref_out, ref_rout = arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, mode=mode)
+    kernel = "stream" if mode == "one_stage" else "auto"
+
+    def call(out=None, rout=None):
+        return arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, w.eps, out=out,
+                                 residual_out=rout, mode=mode, kernel=kernel)[:2]
+
+    ref_out, ref_rout = call()
     s = torch.cuda.Stream()
     out = torch.empty_like(inp.residual)
     rout = torch.empty_like(inp.residual)
@@ -382,8 +412,7 @@ def test_stream_kernel_in_a_graph_matches_eager(mode):
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=s):
         for _ in range(3):
-            arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, w.eps, out=out,
-                           residual_out=rout, mode=mode)
+            call(out, rout)
     out.zero_()
     rout.zero_()
     g.replay()

@@ -12,7 +12,8 @@ sys.path.insert(0, ROOT)
 
 from allreduce_sum_residual_gb300 import plan_table as pt  # noqa: E402
 
-KEYS = ("stream", "register1", "register2", "register4", "register8")
+KEYS = ("stream", "register1", "register2", "register4", "register8", "late1", "late2", "late4",
+        "late8")
 
 
 def _winner(n, H, m):
@@ -50,20 +51,34 @@ def test_keeps_the_fastest_per_cell(tmp_path):
         assert table[cell][0] == chars[_winner(*cell)]
 
 
-def test_averages_repeats(tmp_path):
-    a, b = tmp_path / "a.jsonl", tmp_path / "b.jsonl"
+def test_averages_repeats_within_a_file(tmp_path):
+    a = tmp_path / "a.jsonl"
     _write(a, _grid(), bonus=100.0)
-    # the second run favours another candidate by less than the first's margin
-    with open(b, "w") as f:
+    # a repeated line for every cell favours another candidate by less than
+    # the first line's margin: the average keeps the first winner
+    with open(a, "a") as f:
         for (n, H, m) in _grid():
             row = {"n": n, "H": H, "m": m}
             for k in KEYS:
                 row[k] = 1000.0
             row["stream" if _winner(n, H, m) != "stream" else "register1"] = 1050.0
             f.write(json.dumps(row) + "\n")
-    table = pt.choose(pt.load([str(a), str(b)]))
+    table = pt.choose(pt.load([str(a)]))
     chars = dict(pt.CANDIDATES)
     for cell in _grid():
+        assert table[cell][0] == chars[_winner(*cell)]
+
+
+def test_a_later_file_replaces_whole_cells(tmp_path):
+    a, b = tmp_path / "a.jsonl", tmp_path / "b.jsonl"
+    _write(a, _grid(), bonus=100.0)
+    n0, H0, m0 = _grid()[0]
+    with open(b, "w") as f:   # one cell re-measured with only two candidates
+        f.write(json.dumps({"n": n0, "H": H0, "m": m0, "stream": 900.0, "late2": 1000.0}) + "\n")
+    table = pt.choose(pt.load([str(a), str(b)]))
+    assert table[(n0, H0, m0)] == ("b", [90, 0, 0, 0, 0, 0, 100, 0, 0])
+    chars = dict(pt.CANDIDATES)
+    for cell in _grid()[1:]:
         assert table[cell][0] == chars[_winner(*cell)]
 
 
@@ -79,10 +94,11 @@ def test_percentages(tmp_path):
     with open(f, "w") as fh:
         for (n, H, m) in _grid():
             fh.write(json.dumps({"n": n, "H": H, "m": m, "stream": 500.0, "register1": 1000.0,
-                                 "register2": 995.0, "register4": None, "register8": 333.0}) + "\n")
+                                 "register2": 995.0, "register4": None, "register8": 333.0,
+                                 "late1": 1010.0}) + "\n")
     table = pt.choose(pt.load([str(f)]))
     for cell in _grid():
-        assert table[cell] == ("1", [50, 100, 100, 0, 33])
+        assert table[cell] == ("a", [50, 99, 99, 0, 33, 100, 0, 0, 0])
 
 
 def test_rendered_header_matches_the_grid(tmp_path):
@@ -91,7 +107,7 @@ def test_rendered_header_matches_the_grid(tmp_path):
     table = pt.choose(pt.load([str(f)]))
     text = pt.render(table, 152, "test")
     assert "constexpr int kPlanTableSms = 152;" in text
-    assert f"kPlanScore[{len(INPUTS)}][{len(HIDDEN)}][{len(ROWS)}][5]" in text
+    assert f"kPlanScore[{len(INPUTS)}][{len(HIDDEN)}][{len(ROWS)}][{len(pt.CANDIDATES)}]" in text
     assert "kPlanInputs[6] = {1, 2, 3, 4, 8, 16}" in text
     assert "kPlanPacks[3] = {256, 512, 896}" in text
     assert "kPlanRows[4] = {64, 128, 512, 4096}" in text
@@ -116,7 +132,8 @@ def test_generator_reproduces_the_committed_layout():
     inputs, packs, rows = grab("kPlanInputs"), grab("kPlanPacks"), grab("kPlanRows")
     sms = int(re.search(r"kPlanTableSms = (\d+)", text).group(1))
     body = text[text.index("kPlanScore["):]
-    cells = [[int(x) for x in c.split(",")] for c in re.findall(r"\{(\d+(?:,\d+){4})\}", body)]
+    nc = len(pt.CANDIDATES)
+    cells = [[int(x) for x in c.split(",")] for c in re.findall(r"\{(\d+(?:,\d+){%d})\}" % (nc - 1), body)]
     assert len(cells) == len(inputs) * len(packs) * len(rows)
     chars = [c for _, c in pt.CANDIDATES]
     table, it = {}, iter(cells)

@@ -33,9 +33,10 @@ def _ptxas_registers(src, tmp_path):
             continue
         m = re.search(r"Used (\d+) registers", line)
         if m and entry:
-            k = re.search(r"k_fused_epilogueILi(\d+)ELi(\d+)ELb([01])E", entry)
+            k = re.search(r"k_fused_epilogueILi(\d+)ELi(\d+)ELb([01])ELb([01])E", entry)
             if k:
-                regs[(int(k.group(1)), int(k.group(2)), k.group(3) == "1")] = int(m.group(1))
+                regs[(int(k.group(1)), int(k.group(2)), k.group(3) == "1", k.group(4) == "1")] = \
+                    int(m.group(1))
             entry = None
     return regs
 
@@ -46,8 +47,22 @@ def test_one_cta_register_kernel_fits_two_ctas_per_sm_at_896_threads(tmp_path):
     src = os.path.join(ROOT, "allreduce_sum_residual_gb300", "csrc", "epilogue_g0.cu")
     regs = _ptxas_registers(src, tmp_path)
     for n in (1, 2, 3):
-        assert regs[(n, 1, False)] <= 32, (n, regs[(n, 1, False)])
+        assert regs[(n, 1, False, False)] <= 32, (n, regs[(n, 1, False, False)])
     # 4 inputs: <= 40 keeps three 512-thread CTAs per SM (H = 4096)
-    assert regs[(4, 1, False)] <= 40, regs[(4, 1, False)]
+    assert regs[(4, 1, False, False)] <= 40, regs[(4, 1, False, False)]
     # this translation unit holds only the one-CTA copies (16 of them)
-    assert sorted(regs) == [(n, v, False) for n in (1, 2, 3, 4) for v in (1, 2, 4, 8)]
+    assert sorted(regs) == [(n, v, False, False) for n in (1, 2, 3, 4) for v in (1, 2, 4, 8)]
+
+
+@pytest.mark.skipif(shutil.which("nvcc") is None and not os.path.exists("/usr/local/cuda/bin/nvcc"),
+                    reason="needs nvcc")
+def test_late_weight_kernel_saves_registers(tmp_path):
+    """Loading the weight after the sums frees its registers while the
+    partials are in flight: with 4 inputs at one pack per thread the kernel
+    fits 32 registers, two 896-thread CTAs per SM (H = 7168)."""
+    d = os.path.join(ROOT, "allreduce_sum_residual_gb300", "csrc")
+    late = _ptxas_registers(os.path.join(d, "epilogue_l0.cu"), tmp_path)
+    early = _ptxas_registers(os.path.join(d, "epilogue_g0.cu"), tmp_path)
+    assert sorted(late) == [(n, v, False, True) for n in (1, 2, 3, 4) for v in (1, 2, 4, 8)]
+    assert late[(4, 1, False, True)] <= 32, late[(4, 1, False, True)]
+    assert late[(4, 1, False, True)] < early[(4, 1, False, False)]
