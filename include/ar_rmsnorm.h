@@ -138,8 +138,11 @@ typedef struct {
 /*
  * The plan ar_rmsnorm would follow for (n, m, H, mode) on a GPU with
  * `sm_count` SMs (0: ask the current device).  Pure host logic when
- * sm_count > 0.  Returns AR_OK or AR_ERR_ARG / AR_ERR_ALIGN /
- * AR_ERR_UNSUPPORTED as ar_rmsnorm would.
+ * sm_count > 0: the measured plan table with plain interpolation between
+ * its rows columns.  With sm_count = 0 it is exactly ar_rmsnorm's plan on
+ * the current device, whose interpolation also uses each kernel's occupancy
+ * there (so the two can differ between grid points).  Returns AR_OK or
+ * AR_ERR_ARG / AR_ERR_ALIGN / AR_ERR_UNSUPPORTED as ar_rmsnorm would.
  */
 int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count,
                 ar_plan_t *plan);
