@@ -91,6 +91,33 @@ struct DeviceState {
 static std::mutex g_mu;
 static DeviceState g_dev[kMaxDevices];
 
+// [device][n - 1][log2 vpt][late weight][threads / 32 - 1]: CTAs per SM of
+// the one-CTA register kernels (the driver's occupancy figure), filled when
+// a device is made ready; 0 = unknown.
+static signed char g_occupancy[kMaxDevices][AR_MAX_RANKS][4][2][32];
+
+// Every one-CTA register kernel at every thread count the plan can give it
+// (up to 1024 / vpt), so that planning needs no CUDA call later (it may run
+// inside a graph capture).  About 1900 queries, once per device.
+static void fill_occupancy(int dev) {
+  for (int n = 1; n <= AR_MAX_RANKS; ++n)
+    for (int vl = 0; vl < 4; ++vl)
+      for (int late = 0; late < 2; ++late) {
+        const EpilogueKernel kern = epilogue_kernel(n, 1 << vl, false, late != 0);
+        for (int t = 32; t <= 1024 >> vl; t += 32) {
+          int k = 0;
+          if (kern == nullptr ||
+              cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                  &k, reinterpret_cast<const void *>(kern), t, 0) != cudaSuccess ||
+              k < 0 || k > 64) {
+            cudaGetLastError();
+            k = 0;
+          }
+          g_occupancy[dev][n - 1][vl][late][t / 32 - 1] = static_cast<signed char>(k);
+        }
+      }
+}
+
 // Make the current device ready (SM count, kernel attributes); returns its
 // state or null.  Must run outside graph capture the first time.
 static DeviceState *current_device(int *status) {
@@ -131,6 +158,7 @@ static DeviceState *current_device(int *status) {
           return nullptr;
         }
       }
+    fill_occupancy(dev);
     d.ready = true;
   }
   *status = AR_OK;
@@ -275,11 +303,9 @@ static TableChoice candidate(int c) {
 }
 
 // CTAs of the one-CTA-per-row register kernel (inputs, vpt, late weight)
-// with `threads` threads that fit one SM of the current device: the
-// driver's occupancy figure, cached per device; 0 where it is unknown (no
-// device, or the query failed).
-static signed char g_occupancy[kMaxDevices][AR_MAX_RANKS][4][2][32];
-
+// with `threads` threads that fit one SM of the current device, from the
+// table filled when the device was made ready; 0 where unknown.  No CUDA
+// call here, so planning stays safe inside a graph capture.
 static int device_register_occupancy(int inputs, int vpt, bool late, int threads) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
@@ -290,23 +316,7 @@ static int device_register_occupancy(int inputs, int vpt, bool late, int threads
   if (vl < 0 || inputs < 1 || inputs > AR_MAX_RANKS || threads < 32 || threads > 1024 ||
       threads % 32 != 0)
     return 0;
-  signed char *slot = &g_occupancy[dev][inputs - 1][vl][late ? 1 : 0][threads / 32 - 1];
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (*slot > 0) return *slot;
-  }
-  int k = 0;
-  const EpilogueKernel kern = epilogue_kernel(inputs, vpt, false, late);
-  if (kern == nullptr ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&k, reinterpret_cast<const void *>(kern),
-                                                    threads, 0) != cudaSuccess ||
-      k <= 0 || k > 64) {
-    cudaGetLastError();
-    return 0;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  *slot = static_cast<signed char>(k);
-  return k;
+  return g_occupancy[dev][inputs - 1][vl][late ? 1 : 0][threads / 32 - 1];
 }
 
 using OccupancyFn = int (*)(int inputs, int vpt, bool late, int threads);

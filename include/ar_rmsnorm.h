@@ -45,8 +45,9 @@
  * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream).  No call that launches work synchronises the
  * host or allocates, so the calls may be captured in a CUDA graph.  The
- * first launching call on a device sets kernel attributes; make one call
- * (or ar_reserve_workspace) before capturing.
+ * first launching call on a device sets kernel attributes and reads the
+ * kernels' occupancy for the launch plan; make one call (or
+ * ar_reserve_workspace) before capturing.
  *
  * Aliasing: residual_out may equal residual (in place).  Any other overlap
  * between out, residual_out, residual, the partials and the workspace is
