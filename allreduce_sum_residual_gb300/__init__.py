@@ -18,7 +18,8 @@ Names follow the C ABI:
     ar_load_rmsnorm(temp, residual, weight, eps, out=None, residual_out=None)
     ar_reserve_workspace(max_elems, device) / ar_release_workspace(device)
     ar_workspace_elems(device), ar_select_mode(n, m, H),
-    ar_get_plan(n, m, H, mode, sm_count=0), ar_device_status(device, reset),
+    ar_get_plan(n, m, H, mode, sm_count=0), ar_get_plan_ex(n, m, H, mode, sm_count, ctas_per_sm),
+    ar_device_status(device, reset),
     ar_selftest_bounded_wait(device, limit_us), ar_strerror(status), ar_version()
 """
 import ctypes
@@ -80,6 +81,8 @@ _SIGS = {
                                          ctypes.c_float, _I64, _I64, _VP, _VP, ctypes.c_int, _VP]),
     "ar_get_plan": (ctypes.c_int, [ctypes.c_int, _I64, _I64, ctypes.c_int, ctypes.c_int,
                                    ctypes.POINTER(ar_plan_t)]),
+    "ar_get_plan_ex": (ctypes.c_int, [ctypes.c_int, _I64, _I64, ctypes.c_int, ctypes.c_int,
+                                      _VP, ctypes.POINTER(ar_plan_t)]),
     "ar_reduce_scatter_flat": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _I64, _VP, _VP]),
     "ar_reduce_scatter_store": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _I64, ctypes.c_int,
                                                ctypes.c_int, ctypes.POINTER(_VP), _VP]),
@@ -352,6 +355,21 @@ def ar_get_plan(n, m, H, mode=AR_MODE_AUTO, sm_count=0):
     p = ar_plan_t()
     _check(lib().ar_get_plan(int(n), int(m), int(H), int(MODES.get(mode, mode)), int(sm_count),
                              ctypes.byref(p)), "ar_get_plan")
+    return {f: getattr(p, f) for f, _ in ar_plan_t._fields_}
+
+
+OCCUPANCY_FN = ctypes.CFUNCTYPE(ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int)
+
+
+def ar_get_plan_ex(n, m, H, mode, sm_count, ctas_per_sm=None):
+    """ar_get_plan for a GPU of ``sm_count`` SMs with the caller's occupancy
+    figures: ``ctas_per_sm(inputs, vpt, late_weight, threads) -> int`` (or
+    None for plain interpolation).  Pure host logic."""
+    p = ar_plan_t()
+    fn = OCCUPANCY_FN(lambda a, b, c, d: int(ctas_per_sm(a, b, c, d))) if ctas_per_sm else None
+    _check(lib().ar_get_plan_ex(int(n), int(m), int(H), int(MODES.get(mode, mode)), int(sm_count),
+                                ctypes.cast(fn, _VP) if fn else None, ctypes.byref(p)),
+           "ar_get_plan_ex")
     return {f: getattr(p, f) for f, _ in ar_plan_t._fields_}
 
 

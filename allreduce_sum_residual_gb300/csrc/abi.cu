@@ -306,7 +306,7 @@ static TableChoice candidate(int c) {
 // with `threads` threads that fit one SM of the current device, from the
 // table filled when the device was made ready; 0 where unknown.  No CUDA
 // call here, so planning stays safe inside a graph capture.
-static int device_register_occupancy(int inputs, int vpt, bool late, int threads) {
+static int device_register_occupancy(int inputs, int vpt, int late, int threads) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
@@ -319,7 +319,7 @@ static int device_register_occupancy(int inputs, int vpt, bool late, int threads
   return g_occupancy[dev][inputs - 1][vl][late ? 1 : 0][threads / 32 - 1];
 }
 
-using OccupancyFn = int (*)(int inputs, int vpt, bool late, int threads);
+using OccupancyFn = ar_occupancy_fn;
 
 // `occupancy` (may be null) makes the rows interpolation wave-aware.  A
 // register-kernel candidate runs its rows in waves of (CTAs per SM x SMs);
@@ -344,7 +344,8 @@ static TableChoice table_choice(int inputs, int64_t m, int64_t P, int sms,
     const TableChoice k = candidate(c);
     if (occupancy != nullptr && k.kernel != AR_KERNEL_STREAM && m0 != m1) {
       const int threads = static_cast<int>(((P + k.vpt - 1) / k.vpt + 31) / 32 * 32);
-      const int per_sm = occupancy(inputs, k.vpt, k.kernel == AR_KERNEL_REGISTER_LATE_W, threads);
+      const int per_sm = occupancy(inputs, k.vpt, k.kernel == AR_KERNEL_REGISTER_LATE_W ? 1 : 0,
+                                   threads);
       if (per_sm > 0) {
         const double wave = static_cast<double>(per_sm) * kPlanTableSms;
         const double w = std::ceil(rows / wave);
@@ -820,6 +821,14 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count, ar_plan_t *
     occupancy = device_register_occupancy;
   }
   return make_plan(n, m, H, mode, sm_count, smem, nullptr, plan, occupancy);
+}
+
+int ar_get_plan_ex(int n, int64_t m, int64_t H, int mode, int sm_count,
+                   ar_occupancy_fn ctas_per_sm, ar_plan_t *plan) {
+  if (!plan || sm_count <= 0) return AR_ERR_ARG;
+  const int st = check_shape(n, m, H, 0.f);
+  if (st != AR_OK) return st;
+  return make_plan(n, m, H, mode, sm_count, kAssumedSmemOptin, nullptr, plan, ctas_per_sm);
 }
 
 int ar_device_status(int device, int reset) {

@@ -149,6 +149,24 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count,
                 ar_plan_t *plan);
 
 /*
+ * CTAs per SM of the one-CTA-per-row register kernel for `inputs` partials,
+ * `vpt` packs per thread, the weight loaded late (late_weight = 1) or not,
+ * with `threads` threads per CTA; 0 if unknown.
+ */
+typedef int (*ar_occupancy_fn)(int inputs, int vpt, int late_weight, int threads);
+
+/*
+ * As ar_get_plan with sm_count > 0 (pure host logic, no CUDA call), with the
+ * caller's occupancy figures for the wave-aware interpolation of the plan
+ * table that ar_rmsnorm does with the device's own figures: plan for
+ * another GPU, or test the planner.  ctas_per_sm may be NULL (plain
+ * interpolation).  It is called during the call only.  AR_ERR_ARG for
+ * sm_count <= 0 or a NULL plan.
+ */
+int ar_get_plan_ex(int n, int64_t m, int64_t H, int mode, int sm_count,
+                   ar_occupancy_fn ctas_per_sm, ar_plan_t *plan);
+
+/*
  * As ar_rmsnorm, with two additions for testing and tuning:
  *   sum_out  [m, H] fp32 device buffer (16-byte aligned) that receives the
  *            reduced sum feeding the residual add: the fp32 accumulator for

@@ -302,6 +302,72 @@ def test_plan_between_grid_points(arlib):
         assert _expect(p, ch), (n, m, H, mode, sm, ch, p)
 
 
+def _table_pick_waves(grid, sms_table, score, n, m, P, sms, occ):
+    """The wave-aware lookup restated: per candidate, a register kernel's
+    rows columns are narrowed to those in the shape's own wave count (waves
+    of occ(...) x the table's SMs, rows scaled to the table's SMs); the best
+    mean percentage wins (first on ties)."""
+    import math
+    n0, n1 = _bracket(grid["kPlanInputs"], n)
+    p0, p1 = _bracket(grid["kPlanPacks"], P)
+    rows = m * sms_table / sms
+    m0, m1 = _bracket(grid["kPlanRows"], rows)
+    nc = len(score[0][0][0])
+    best, best_mean = 0, -1.0
+    for c in range(nc):
+        lo, hi = m0, m1
+        if c > 0 and m0 != m1:
+            vpt = 1 << ((c - 1) % 4)
+            late = 1 if c >= 5 else 0
+            threads = -(-(-(-P // vpt)) // 32) * 32
+            k = occ(n, vpt, late, threads)
+            if k > 0:
+                wave = k * sms_table
+                w = math.ceil(rows / wave)
+                at_lo = math.ceil(grid["kPlanRows"][m0] / wave) == w
+                at_hi = math.ceil(grid["kPlanRows"][m1] / wave) == w
+                if at_lo and not at_hi:
+                    hi = m0
+                if at_hi and not at_lo:
+                    lo = m1
+        vals = [score[i][j][k2][c] for i in range(n0, n1 + 1) for j in range(p0, p1 + 1)
+                for k2 in range(lo, hi + 1)]
+        mean = sum(vals) / len(vals)
+        if mean > best_mean:
+            best, best_mean = c, mean
+    return _cand_char(best)
+
+
+def test_wave_aware_plan_with_given_occupancy(arlib):
+    """ar_get_plan_ex with a fake occupancy (CTAs per SM from a made-up
+    register count per (inputs, vpt, late)) equals the restated wave-aware
+    lookup on random shapes; without occupancy it is ar_get_plan."""
+    import random
+    grid, sms, score = plan_table()
+
+    def occ(inputs, vpt, late, threads):
+        regs = 24 + 4 * inputs * vpt - (4 * vpt if late else 0)
+        regs = (min(regs, 255) + 7) // 8 * 8
+        return max(1, min(65536 // (threads * regs), 2048 // threads, 32))
+
+    rng = random.Random(11)
+    differ = 0
+    for _ in range(2000):
+        n = rng.randint(1, 16)
+        H = 8 * rng.randint(4, grid["kPlanPacks"][-1])
+        m = int(round(10 ** rng.uniform(1.81, 4.4)))
+        sm = rng.choice((sms, 132, 160))
+        p = arlib.ar_get_plan_ex(n, m, H, 1, sm, occ)
+        ch = _table_pick_waves(grid, sms, score, n, m, H // 8, sm, occ)
+        assert _expect(p, ch), (n, m, H, sm, ch, p)
+        plain = arlib.ar_get_plan_ex(n, m, H, 1, sm, None)
+        assert plain == arlib.ar_get_plan(n, m, H, 1, sm_count=sm)
+        differ += plain != p
+    assert differ > 0   # the waves do change some choices
+    with pytest.raises(arlib.ArError):
+        arlib.ar_get_plan_ex(4, 100, 4096, 1, 0, occ)
+
+
 def test_plan_rejects_bad_shapes(arlib):
     with pytest.raises(arlib.ArError):
         arlib.ar_get_plan(8, 4, 1020, 1, sm_count=152)
