@@ -183,7 +183,9 @@ int ar_get_plan_ex(int n, int64_t m, int64_t H, int mode, int sm_count,
  *            memory is short), `ctas` = grid size (several CTAs per SM split
  *            its shared memory).  Other combinations return AR_ERR_ARG;
  *            `mode` and `launches` are ignored (`mode` argument picks the
- *            path).  The results do not depend on the kernel or the shape.
+ *            path).  The sum and residual_out do not depend on the kernel or
+ *            the shape; out may differ in its last bit between shapes (the
+ *            square sum is reduced in a shape-dependent order).
  */
 int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
                   const void *weight, float eps, int64_t m, int64_t H,
