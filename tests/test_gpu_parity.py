@@ -472,6 +472,57 @@ def test_device_plan_respects_wave_boundaries():
     assert arn.ar_get_plan(4, 256, 7168, 1) == arn.ar_get_plan(4, 256, 7168, 1, sm_count=sms)
 
 
+def _plant_nonfinite(inp, rng):
+    """Plant +inf, -inf and NaN in a few partial and residual elements
+    (bf16 patterns), one kind per chosen row; returns the planted rows."""
+    m, H = inp.residual.shape
+    rows = rng.choice(m, size=min(m, 6), replace=False)
+    pats = [0x7F80, 0xFF80, 0x7FC0]
+    for i, r in enumerate(rows):
+        col = int(rng.integers(H))
+        t = inp.partials[i % len(inp.partials)] if i % 2 == 0 else inp.residual
+        t.view(torch.int16)[r, col] = torch.tensor(pats[i % 3], dtype=torch.int32).to(torch.int16)
+    return rows
+
+
+def _compare_nonfinite(gpu, orc, tag):
+    """NaN where the oracle has NaN (any payload), every other element as in
+    compare(): sum and residual_out bit-exact, out within the tolerance."""
+    g_out, g_rout, g_sum = gpu
+    o_out, o_rout, o_sum = orc
+    gs = g_sum.cpu().numpy()
+    assert np.array_equal(np.isnan(gs), np.isnan(o_sum)), tag
+    ok = ~np.isnan(o_sum)
+    assert np.array_equal(gs[ok].view(np.uint32), o_sum[ok].view(np.uint32)), tag
+    gr, orr = to_f32(synth.bits(g_rout)), to_f32(o_rout)
+    assert np.array_equal(np.isnan(gr), np.isnan(orr)), tag
+    ok = ~np.isnan(orr)
+    assert np.array_equal(synth.bits(g_rout)[ok], o_rout[ok]), tag
+    go, oo = to_f32(synth.bits(g_out)).astype(np.float64), to_f32(o_out).astype(np.float64)
+    assert np.array_equal(np.isnan(go), np.isnan(oo)), tag
+    ok = ~np.isnan(oo)
+    assert np.all(np.abs(go[ok] - oo[ok]) <= 2.0 ** -7 * np.abs(oo[ok]) + 1e-3), tag
+
+
+@pytest.mark.parametrize("m,kernel,mode", [(40, 0, "one_stage"), (300, 0, "one_stage"),
+                                           (300, "stream", "one_stage"),
+                                           (300, "register_late", "one_stage"),
+                                           (300, 0, "two_stage")])
+def test_inf_and_nan_propagate_as_in_the_oracle(m, kernel, mode):
+    """Non-finite inputs are not special-cased: inf and NaN flow through the
+    sum, residual_out and the norm (a row with an inf gets inv = 0, one with
+    a NaN is NaN throughout), exactly as in the oracle."""
+    w = synth.Workload("nonfinite", n=3, H=7168, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m, seed=21)
+    rows = _plant_nonfinite(inp, np.random.default_rng(5))
+    cluster = 1 if kernel == "register_late" else 0
+    gpu = run_gpu(inp, mode, cluster=cluster, kernel=kernel)
+    torch.cuda.synchronize()
+    orc = oracle_rows(inp, None, mode == "two_stage")
+    assert np.isnan(to_f32(orc[0][rows])).any()   # the plant reached the outputs
+    _compare_nonfinite(gpu, orc, f"non-finite m={m} {kernel} {mode}")
+
+
 def test_raw_c_abi_call():
     """The plain C entry point with raw pointers (no binding helpers)."""
     w = synth.TINY
