@@ -1,0 +1,77 @@
+"""bench.py's host helpers, without a GPU: the byte counts behind every GB/s
+figure, the peak lookup, the source-hash gate on recorded ncu traffic, and
+the argument checks of the command line."""
+import json
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_algorithmic_bytes_match_the_scope_formula():
+    # (n + 3) m H 2 + 2 H: n partials and the residual read, out and
+    # residual_out written, the weight read once
+    assert bench.algo_bytes(8, 8192, 6144) == 1_107_308_544
+    assert bench.algo_bytes(2, 4, 1024) == 43_008
+    assert bench.algo_bytes(8, 1, 7168) == 172_032
+    for n, m, H in ((1, 1, 8), (16, 3, 131072), (4, 2048, 7168)):
+        assert bench.algo_bytes(n, m, H) == ((n + 3) * m + 1) * H * 2
+
+
+def test_two_stage_moves_the_temporary_twice_more():
+    n, m, H = 4, 2048, 7168
+    assert bench.actual_bytes(n, m, H, False) == bench.algo_bytes(n, m, H)
+    assert bench.actual_bytes(n, m, H, True) == (n + 5) * m * H * 2 + H * 2
+
+
+def test_peak_comes_from_the_measured_file_or_the_fallback(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.peaks() == (bench.FALLBACK_HBM_GBS, "of fallback")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6690.5}))
+    assert bench.peaks() == (6690.5, "of measured")
+
+
+def test_recorded_traffic_is_dropped_once_the_kernel_sources_change(tmp_path, monkeypatch):
+    csrc = tmp_path / "allreduce_sum_residual_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    (tmp_path / "profiles").mkdir()
+    for name in ("common.cuh", "stream_epilogue.cuh"):
+        (csrc / name).write_text(f"// {name}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    h = bench.source_hash("k_stream_epilogue")
+    rec = {"k_stream_epilogue@prefill": {"source_hash": h, "dram_bytes_per_launch": 1084702208}}
+    (tmp_path / "profiles" / "ncu_traffic.json").write_text(json.dumps(rec))
+    assert bench.ncu_traffic("k_stream_epilogue", "prefill") == 1084702208.0
+    assert bench.ncu_traffic("k_stream_epilogue", "decode") is None      # no capture
+    (csrc / "stream_epilogue.cuh").write_text("// changed\n")
+    assert bench.source_hash("k_stream_epilogue") != h
+    assert bench.ncu_traffic("k_stream_epilogue", "prefill") is None     # stale
+
+
+def test_committed_traffic_record_matches_the_current_stream_kernel():
+    """The prefill traffic figure the bench reports is only valid for the
+    kernel it was captured from; the record must carry the current hash."""
+    with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+        rec = json.load(f)
+    e = rec["k_stream_epilogue@prefill"]
+    assert e["source_hash"] == bench.source_hash("k_stream_epilogue")
+    assert 0.9 * bench.algo_bytes(8, 8192, 6144) < e["dram_bytes_per_launch"] < \
+        1.1 * bench.algo_bytes(8, 8192, 6144)
+
+
+def test_warmup_below_three_is_refused():
+    with pytest.raises(SystemExit):
+        bench.main(["--warmup", "2"])
+
+
+def test_every_kernel_candidate_names_a_forced_shape():
+    for name, shape in bench.KERNEL_CANDIDATES.items():
+        kernel, cluster, vpt = shape
+        assert kernel in ("stream", "register", "register_late")
+        assert (vpt == 0) == (kernel == "stream")
+        assert name.endswith(str(vpt)) or kernel == "stream"
