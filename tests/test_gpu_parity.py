@@ -205,8 +205,12 @@ def guarded(m, H):
 
 
 @pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
-@pytest.mark.parametrize("m,H", [(1, 8), (7, 1032), (19, 7168)])
-def test_outputs_stay_inside_their_buffers(mode, m, H):
+@pytest.mark.parametrize("m,H", [(1, 8), (7, 1032), (19, 7168), (300, 4104)])
+@pytest.mark.parametrize("kernel,cluster", [(0, 0), ("stream", 0), ("register_late", 1),
+                                            ("register", 4)])
+def test_outputs_stay_inside_their_buffers(mode, m, H, kernel, cluster):
+    """Canaries around every output, for every kernel form (the plan's
+    choice, the stream kernel, the late-weight kernel, a forced cluster)."""
     w = synth.Workload("guard", n=4, H=H, ms=(m,), p_std=0.5, res_std=1.0)
     inp = device_inputs(w, m)
     bo, out, g = guarded(m, H)
@@ -214,7 +218,7 @@ def test_outputs_stay_inside_their_buffers(mode, m, H):
     bs = torch.full((m * H + 2 * 1024,), 7.0, dtype=torch.float32, device="cuda")
     s = bs[1024:1024 + m * H].view(m, H)
     arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, inp.eps, out=out, residual_out=rout,
-                      mode=mode, sum_out=s)
+                      mode=mode, sum_out=s, kernel=kernel, cluster=cluster)
     torch.cuda.synchronize()
     for b in (bo, br):
         assert torch.all(b[:g] == 0x5A5A) and torch.all(b[g + m * H:] == 0x5A5A)
