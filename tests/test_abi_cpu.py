@@ -152,10 +152,8 @@ SHAPES = [(2, 4, 1024), (8, 1, 7168), (8, 16, 7168), (4, 32, 7168), (4, 2048, 71
           (3, 1000, 65536), (8, 151, 7168), (8, 152, 7168), (8, 304, 7168)]
 
 
-@pytest.mark.parametrize("n,m,H", SHAPES)
-@pytest.mark.parametrize("mode", [0, 1, 2])
-def test_plan_covers_every_pack(arlib, n, m, H, mode):
-    p = arlib.ar_get_plan(n, m, H, mode, sm_count=152)
+def _check_plan(p, n, m, H, mode):
+    """What every plan must satisfy, whatever the table chose."""
     P = H // 8
     assert p["mode"] in (1, 2) and (mode == 0 or p["mode"] == mode)
     assert p["launches"] == (2 if p["mode"] == 2 else 1)
@@ -163,6 +161,7 @@ def test_plan_covers_every_pack(arlib, n, m, H, mode):
     if p["kernel"] in (1, 3):   # register kernel: one CTA or a cluster per row
         per_cta = -(-P // p["cluster"])
         assert p["cluster"] in (1, 2, 4, 8, 16) and p["stages"] == 0
+        assert p["kernel"] == 1 or p["cluster"] == 1              # late weight: one CTA per row
         assert p["threads"] % 32 == 0 and 32 <= p["threads"] <= 1024 // p["vpt"]
         assert p["threads"] * p["vpt"] >= per_cta          # every pack has an owner
         assert per_cta <= 1024                             # a row slice fits in registers
@@ -178,6 +177,26 @@ def test_plan_covers_every_pack(arlib, n, m, H, mode):
         per_sm = -(-p["ctas"] // 152)
         assert 2 <= p["stages"] <= 16 and per_sm * (smem + 1024) <= 233472
         assert p["ctas"] in (min(m, 152), min(m, 304))
+
+
+@pytest.mark.parametrize("n,m,H", SHAPES)
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_plan_covers_every_pack(arlib, n, m, H, mode):
+    _check_plan(arlib.ar_get_plan(n, m, H, mode, sm_count=152), n, m, H, mode)
+
+
+def test_every_table_cell_plans_a_launchable_shape(arlib):
+    """At every grid point of the plan table, and half-way between rows
+    columns, both modes give a plan that satisfies the launch constraints."""
+    grid, sms, _ = plan_table()
+    rows = grid["kPlanRows"]
+    between = [(a + b) // 2 for a, b in zip(rows, rows[1:])]
+    for n in grid["kPlanInputs"]:
+        for P in grid["kPlanPacks"]:
+            for m in rows + between:
+                for mode in (1, 2):
+                    _check_plan(arlib.ar_get_plan(n, m, 8 * P, mode, sm_count=sms), n, m, 8 * P,
+                                mode)
 
 
 def test_plan_spreads_small_batches(arlib):
