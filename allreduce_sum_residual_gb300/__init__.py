@@ -34,6 +34,7 @@ AR_ERR_CUDA = 5
 AR_ERR_TIMEOUT = 6
 AR_ERR_UNSUPPORTED = 7
 AR_ERR_SCRATCH_LIMIT = 8
+AR_ERR_BOUNDS = 9
 AR_STATIC_SCRATCH_ELEMS = 8 * 1024 * 1024
 
 AR_MODE_AUTO = 0
@@ -61,10 +62,18 @@ KERNELS = {"auto": AR_KERNEL_AUTO, "register": AR_KERNEL_REGISTER, "stream": AR_
            "register_late": AR_KERNEL_REGISTER_LATE_W}
 
 
+AR_PREFETCH_AUTO = 0
+AR_PREFETCH_NONE = 1
+AR_PREFETCH_ROW = 2
+AR_PREFETCH_ROW_AHEAD = 3
+PREFETCHES = {"auto": AR_PREFETCH_AUTO, "none": AR_PREFETCH_NONE, "row": AR_PREFETCH_ROW,
+              "row_ahead": AR_PREFETCH_ROW_AHEAD}
+
+
 class ar_plan_t(ctypes.Structure):
     _fields_ = [("mode", ctypes.c_int), ("kernel", ctypes.c_int), ("cluster", ctypes.c_int),
                 ("vpt", ctypes.c_int), ("threads", ctypes.c_int), ("stages", ctypes.c_int),
-                ("ctas", ctypes.c_int64), ("launches", ctypes.c_int)]
+                ("ctas", ctypes.c_int64), ("launches", ctypes.c_int), ("prefetch", ctypes.c_int)]
 
 
 _lib = None
@@ -95,9 +104,35 @@ _SIGS = {
                                                    ctypes.c_float, _I64, _I64, _VP, _VP, _VP]),
     "ar_device_status": (ctypes.c_int, [ctypes.c_int, ctypes.c_int]),
     "ar_selftest_bounded_wait": (ctypes.c_int, [ctypes.c_int, ctypes.c_uint]),
+    "ar_signal_post": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int,
+                                      ctypes.c_uint32, _VP]),
+    "ar_signal_wait": (ctypes.c_int, [_VP, ctypes.c_int, ctypes.c_uint32, ctypes.c_uint, _VP]),
+    "ar_barrier": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, ctypes.c_int, ctypes.c_uint32,
+                                  ctypes.c_uint, _VP]),
+    "ar_rmsnorm_two_shot": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP,
+                                           ctypes.c_float, _I64, _I64, _VP, _VP, ctypes.c_int,
+                                           ctypes.c_int, ctypes.POINTER(_VP), ctypes.POINTER(_VP),
+                                           ctypes.c_uint32, ctypes.c_uint, _VP]),
+    "ar_ipc_get_handle": (ctypes.c_int, [_VP, ctypes.c_char_p, ctypes.POINTER(_I64)]),
+    "ar_ipc_open": (ctypes.c_int, [ctypes.c_char_p, _I64, ctypes.POINTER(_VP)]),
+    "ar_ipc_close": (ctypes.c_int, [ctypes.c_char_p]),
+    "ar_selftest_barrier": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint,
+                                           ctypes.POINTER(ctypes.c_int)]),
+    "ar_checks_bounds": (ctypes.c_int, []),
+    "ar_selftest_bounds": (ctypes.c_int, [ctypes.c_int]),
     "ar_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "ar_version": (ctypes.c_int, []),
 }
+
+
+def load(path):
+    """A build of the library at `path` (ctypes), with argument types set."""
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
 
 
 def lib():
@@ -108,12 +143,7 @@ def lib():
             raise RuntimeError(
                 f"{LIB_PATH} is not built: run `python -c \"import __graft_entry__ as g; g.build()\"`"
                 " (the CUDA library is required; there is no fallback)")
-        handle = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = handle
+        _lib = load(LIB_PATH)
     return _lib
 
 
@@ -253,12 +283,13 @@ def ar_rmsnorm_mapped(partials, residual, weight, eps, out=None, residual_out=No
 
 def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
                   mode=AR_MODE_AUTO, stream=None, sum_out=None, cluster=0, vpt=0, kernel=0,
-                  threads=0, stages=0, ctas=0):
+                  threads=0, stages=0, ctas=0, prefetch=0):
     """ar_rmsnorm plus the reduced sum (fp32 [m, H] ``sum_out``) and a forced
     kernel ("register" / "register_late" / "stream") and launch shape: register kernel
     ``cluster`` CTAs per row and ``vpt`` packs per thread; stream kernel
-    ``threads`` (32 + consumers), ring ``stages`` and grid ``ctas``.  0 =
-    library's choice.  Returns (out, residual_out, sum_out)."""
+    ``threads`` (32 + consumers), ring ``stages`` and grid ``ctas``; L2
+    ``prefetch`` ("none" / "row" / "row_ahead").  0 = library's choice.
+    Returns (out, residual_out, sum_out)."""
     import torch
     mode = MODES.get(mode, mode)
     m, H, dev, out, residual_out, arr = _prepare(partials, residual, weight, out, residual_out)
@@ -268,9 +299,10 @@ def ar_rmsnorm_ex(partials, residual, weight, eps, out=None, residual_out=None,
             raise ValueError("sum_out must be a contiguous float32 [m, H] tensor on the inputs' device")
     plan = None
     kernel = KERNELS.get(kernel, kernel)
-    if cluster or vpt or kernel or threads or stages or ctas:
+    prefetch = PREFETCHES.get(prefetch, prefetch)
+    if cluster or vpt or kernel or threads or stages or ctas or prefetch:
         plan = ctypes.pointer(ar_plan_t(0, int(kernel), int(cluster), int(vpt), int(threads),
-                                        int(stages), int(ctas), 0))
+                                        int(stages), int(ctas), 0, int(prefetch)))
     st = lib().ar_rmsnorm_ex(arr, len(partials), _ptr(residual), _ptr(weight), float(eps), m, H,
                              _ptr(out), _ptr(residual_out), int(mode), _stream_ptr(stream, dev),
                              _VP(sum_out.data_ptr()) if sum_out is not None else None, plan)
@@ -382,6 +414,100 @@ def ar_device_status(device=0, reset=False):
 def ar_selftest_bounded_wait(device=0, limit_us=1000):
     """Run the bounded-wait self-test kernel; returns the status it left."""
     return int(lib().ar_selftest_bounded_wait(int(device), int(limit_us)))
+
+
+# ---------------------------------------------------------------- cross-rank data plane
+
+AR_SIGNAL_PAD_BYTES = AR_MAX_RANKS * 4
+AR_IPC_HANDLE_BYTES = 64
+
+
+def _addr(x):
+    """A device address from a tensor or an int."""
+    return int(x.data_ptr()) if hasattr(x, "data_ptr") else int(x)
+
+
+def _addrs(xs):
+    return (_VP * len(xs))(*[_addr(x) for x in xs])
+
+
+def _cur_stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return _VP(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def ar_signal_post(pads, rank, epoch, stream=None):
+    """Post `epoch` of `rank` into every rank's signal pad (tensors or addresses)."""
+    _check(lib().ar_signal_post(_addrs(pads), len(pads), int(rank), int(epoch) & 0xFFFFFFFF,
+                                _cur_stream(stream)), "ar_signal_post")
+
+
+def ar_signal_wait(pad, world, epoch, limit_us=1000000, stream=None):
+    """Wait (bounded) until flags 0..world-1 of `pad` reach `epoch`."""
+    _check(lib().ar_signal_wait(_VP(_addr(pad)), int(world), int(epoch) & 0xFFFFFFFF,
+                                int(limit_us), _cur_stream(stream)), "ar_signal_wait")
+
+
+def ar_barrier(pads, rank, epoch, limit_us=1000000, stream=None):
+    """Post, then wait on pads[rank]: a bounded barrier of len(pads) ranks."""
+    _check(lib().ar_barrier(_addrs(pads), len(pads), int(rank), int(epoch) & 0xFFFFFFFF,
+                            int(limit_us), _cur_stream(stream)), "ar_barrier")
+
+
+def ar_rmsnorm_two_shot(partials, residual, weight, eps, temps, pads, rank, epoch, out=None,
+                        residual_out=None, limit_us=1000000, stream=None):
+    """Two-stage epilogue of rank `rank` of len(temps) ranks: its stage-1 slice
+    stored into every rank's temporary, a barrier, stage 2 on temps[rank].
+    `partials`, `temps` and `pads` are tensors or device addresses (peer or
+    IPC mappings for other ranks); residual, weight and the outputs are
+    tensors of this device.  Returns (out, residual_out)."""
+    import torch
+    m, H = residual.shape
+    _check_tensor(residual, "residual", (m, H), None)
+    _check_tensor(weight, "weight", (H,), residual.device)
+    if out is None:
+        out = torch.empty_like(residual)
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    _check_tensor(out, "out", (m, H), residual.device)
+    _check_tensor(residual_out, "residual_out", (m, H), residual.device)
+    st = lib().ar_rmsnorm_two_shot(_addrs(partials), len(partials), _ptr(residual), _ptr(weight),
+                                   float(eps), m, H, _ptr(out), _ptr(residual_out), int(rank),
+                                   len(temps), _addrs(temps), _addrs(pads),
+                                   int(epoch) & 0xFFFFFFFF, int(limit_us),
+                                   _stream_ptr(stream, residual.device))
+    _check(st, "ar_rmsnorm_two_shot")
+    return out, residual_out
+
+
+def ar_ipc_get_handle(x):
+    """(handle bytes, byte offset) of the allocation holding tensor/address x."""
+    h = ctypes.create_string_buffer(AR_IPC_HANDLE_BYTES)
+    off = _I64(0)
+    _check(lib().ar_ipc_get_handle(_VP(_addr(x)), h, ctypes.byref(off)), "ar_ipc_get_handle")
+    return h.raw, int(off.value)
+
+
+def ar_ipc_open(handle, offset):
+    """Device address of byte `offset` of another process's allocation."""
+    p = _VP()
+    _check(lib().ar_ipc_open(bytes(handle), int(offset), ctypes.byref(p)), "ar_ipc_open")
+    return int(p.value)
+
+
+def ar_ipc_close(handle):
+    _check(lib().ar_ipc_close(bytes(handle)), "ar_ipc_close")
+
+
+def ar_selftest_barrier(device=0, world=8, rounds=1000, limit_us=1000000):
+    """All ranks of a barrier in one cooperative kernel; returns (status,
+    stale reads)."""
+    mism = ctypes.c_int(-1)
+    st = int(lib().ar_selftest_barrier(int(device), int(world), int(rounds), int(limit_us),
+                                       ctypes.byref(mism)))
+    return st, int(mism.value)
 
 
 def ar_strerror(status):

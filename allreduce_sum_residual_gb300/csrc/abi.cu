@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "epilogue.cuh"
+#include "peer.cuh"
 #include "plan_table.cuh"
 #include "stream_epilogue.cuh"
 
@@ -34,6 +35,7 @@ StreamKernel stream_kernel_group1(int n, int vpt_log2);
 StreamKernel stream_kernel_group2(int n, int vpt_log2);
 StreamKernel stream_kernel_group3(int n, int vpt_log2);
 cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int *status, cudaStream_t s);
+cudaError_t launch_bounds_selftest(int *status, cudaStream_t s);
 
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far above any legitimate wait
 constexpr int kAssumedSmemOptin = 232448;         // sm_100-class opt-in per CTA (host-only plans)
@@ -188,6 +190,9 @@ static int check_shape(int n, int64_t m, int64_t H, float eps) {
   if (m > (int64_t{1} << 40) / H) return AR_ERR_UNSUPPORTED;  // keeps every byte count in range
   return AR_OK;
 }
+
+// check_shape for the entry points defined in other translation units.
+int check_call_shape(int n, int64_t m, int64_t H, float eps) { return check_shape(n, m, H, eps); }
 
 // Pointers of a full epilogue call: null, alignment, then overlaps.
 static int check_buffers(const void *const *partials, int n, const void *residual,
@@ -487,6 +492,31 @@ static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_opti
   return true;
 }
 
+// CTAs of a one-CTA-per-row register-kernel plan that run at once on the
+// device (its occupancy x SMs); 0 if unknown or not that kind of plan.
+static int64_t resident_ctas(const ar_plan_t &pl, int inputs, int sms, OccupancyFn occupancy) {
+  if (occupancy == nullptr || pl.cluster != 1 || pl.kernel == AR_KERNEL_STREAM) return 0;
+  const int per_sm =
+      occupancy(inputs, pl.vpt, pl.kernel == AR_KERNEL_REGISTER_LATE_W ? 1 : 0, pl.threads);
+  return per_sm > 0 ? static_cast<int64_t>(per_sm) * sms : 0;
+}
+
+// L2 prefetch of the epilogue kernel, measured on GB300 (cold buffers,
+// graphs of back-to-back calls).  Every kernel prefetches its first row
+// (slice) before it waits for the previous grid: decode m = 1 went from
+// 2.05 to 1.74 us per call, n = 4, H = 4096, m = 256 from 3.97 to 2.93 us,
+// the stream kernel gained 1-3 % at 512-1024 rows.  A register kernel whose
+// rows need more than one wave of CTAs also prefetches the row one wave
+// ahead (n = 4, H = 7168, m = 1024: 6.8 -> 7.15 TB/s).  The stream kernel
+// does not prefetch ahead: its ring already runs ahead, and an extra row of
+// prefetches in flight cost it 10-25 %.
+static int plan_prefetch(const ar_plan_t &pl, int64_t m, int inputs, int sms,
+                         OccupancyFn occupancy) {
+  if (pl.kernel == AR_KERNEL_STREAM) return AR_PREFETCH_ROW;
+  const int64_t wave = resident_ctas(pl, inputs, sms, occupancy);
+  return wave > 0 && m > wave ? AR_PREFETCH_ROW_AHEAD : AR_PREFETCH_ROW;
+}
+
 static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
                      const ar_plan_t *force, ar_plan_t *pl, OccupancyFn occupancy = nullptr) {
   if (mode != AR_MODE_AUTO && mode != AR_MODE_ONE_STAGE && mode != AR_MODE_TWO_STAGE)
@@ -509,6 +539,9 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
       return AR_ERR_ARG;
     if (force->threads < 0 || force->stages < 0 || force->stages > 16 || force->ctas < 0)
       return AR_ERR_ARG;
+    if (force->prefetch < AR_PREFETCH_AUTO || force->prefetch > AR_PREFETCH_ROW_AHEAD)
+      return AR_ERR_ARG;
+    if (force->prefetch == AR_PREFETCH_ROW_AHEAD && fc > 1) return AR_ERR_ARG;
   }
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
@@ -534,6 +567,11 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   }
   if (pl->ctas > INT32_MAX) return AR_ERR_UNSUPPORTED;
   pl->launches = pl->mode == AR_MODE_TWO_STAGE ? 2 : 1;
+  pl->prefetch = plan_prefetch(*pl, m, inputs, sms, occupancy);
+  if (force && force->prefetch != AR_PREFETCH_AUTO) {
+    if (force->prefetch == AR_PREFETCH_ROW_AHEAD && pl->cluster > 1) return AR_ERR_ARG;
+    pl->prefetch = force->prefetch;
+  }
   return AR_OK;
 }
 
@@ -565,6 +603,9 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
   cfg.numAttrs = na;
   EpilogueArgs args = a;
   args.early_reads = after_prior ? 1 : 0;
+  // Stage 2 loads its residual and weight before the wait instead; its
+  // input (the temporary) is being written by stage 1 until then.
+  if (after_prior) args.prefetch_own = 0;
   const cudaError_t e = cudaLaunchKernelEx(
       &cfg, epilogue_kernel(n, pl.vpt, pl.cluster > 1, pl.kernel == AR_KERNEL_REGISTER_LATE_W), args);
   if (e != cudaSuccess) return e;
@@ -592,12 +633,16 @@ static cudaError_t launch_stream(const void *const *inputs, int n, const void *r
   a.eps = eps;
   a.wait_limit_ns = kWaitLimitNs;
   a.status = status;
+  // Stage 2 reads the temporary stage 1 is still writing until the wait.
+  a.prefetch_first = !after_prior && (pl.prefetch == AR_PREFETCH_ROW ||
+                                      pl.prefetch == AR_PREFETCH_ROW_AHEAD);
+  a.prefetch_next = pl.prefetch == AR_PREFETCH_ROW_AHEAD;
+  a.smem_bytes = static_cast<int>(stream_smem_bytes(n, Tc, pl.stages));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(pl.ctas), 1, 1);
   cfg.blockDim = dim3(static_cast<unsigned>(pl.threads), 1, 1);
   cfg.dynamicSmemBytes = static_cast<size_t>(stream_smem_bytes(n, Tc, pl.stages));
   cfg.stream = stream;
-  (void)after_prior;  // the stream kernel waits on the previous grid before any global access
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -626,6 +671,20 @@ static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n
   a->eps = eps;
   a->wait_limit_ns = kWaitLimitNs;
   a->status = status;
+  a->prefetch_own = pl.prefetch == AR_PREFETCH_ROW || pl.prefetch == AR_PREFETCH_ROW_AHEAD;
+  a->ahead = 0;
+  if (pl.prefetch == AR_PREFETCH_ROW_AHEAD && pl.cluster == 1) {
+    int sms = 0;
+    const DeviceState *d = nullptr;
+    int dev = -1;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && g_dev[dev].ready) {
+      d = &g_dev[dev];
+      sms = d->sms;
+    } else {
+      cudaGetLastError();
+    }
+    if (d != nullptr) a->ahead = resident_ctas(pl, n, sms, device_register_occupancy);
+  }
 }
 
 // True if the current device `dev` can use `p` at the same address: its own
@@ -640,7 +699,15 @@ static bool device_accessible(const void *p, int dev) {
     return false;
   }
   switch (at.type) {
-    case cudaMemoryTypeDevice: return at.device == dev;
+    case cudaMemoryTypeDevice: {
+      if (at.device == dev) return true;  // this device's memory, or another process's (IPC)
+      int can = 0;                        // another GPU's memory through a peer mapping
+      if (cudaDeviceCanAccessPeer(&can, dev, at.device) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+      }
+      return can != 0;
+    }
     case cudaMemoryTypeManaged: return true;
     case cudaMemoryTypeHost: return at.devicePointer == p;
     default: return false;
@@ -682,6 +749,7 @@ static int run(const void *const *partials, int n, const void *residual, const v
     if (st != AR_OK) return st;
     std::memset(&register_only, 0, sizeof register_only);
     register_only.kernel = AR_KERNEL_REGISTER;
+    register_only.prefetch = AR_PREFETCH_NONE;  // bulk prefetches stay on device memory
     force = &register_only;
   }
   DeviceState *d = current_device(&st);
@@ -727,6 +795,8 @@ static int run(const void *const *partials, int n, const void *residual, const v
   ra.ndst = 1;
   ra.begin = 0;
   ra.end = m * H / kPackElems;
+  ra.prefetch = pl.prefetch != AR_PREFETCH_NONE;
+  ra.status = d->status;
   if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   const void *temp_in[1] = {ws};
   return epilogue(temp_in, 1, true);
@@ -765,6 +835,8 @@ int two_stage_with_temp(const void *const *partials, int n, const void *residual
   ra.ndst = 1;
   ra.begin = 0;
   ra.end = m * H / kPackElems;
+  ra.prefetch = pl.prefetch != AR_PREFETCH_NONE;
+  ra.status = d->status;
   if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   const void *temp_in[1] = {temp};
   cudaError_t e;
@@ -877,6 +949,23 @@ int ar_selftest_bounded_wait(int device, unsigned limit_us) {
   return ar_device_status(device, 1);
 }
 
+int ar_selftest_bounds(int device) {
+  if (device < 0 || device >= kMaxDevices) return AR_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  int st = AR_OK;
+  DeviceState *d = current_device(&st);
+  if (d && launch_bounds_selftest(d->status, nullptr) != cudaSuccess) st = AR_ERR_CUDA;
+  cudaSetDevice(prev);
+  if (st != AR_OK) return st;
+  return ar_device_status(device, 1);
+}
+
+int ar_checks_bounds(void) { return AR_CHECK ? 1 : 0; }
+
 int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count, void *temp,
                            void *stream) {
   if (n < 1 || n > AR_MAX_RANKS || count < 0) return AR_ERR_ARG;
@@ -901,6 +990,8 @@ int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count, vo
   ra.ndst = 1;
   ra.begin = 0;
   ra.end = count / kPackElems;
+  ra.prefetch = 1;
+  ra.status = d->status;
   return launch_reduce_flat(ra, n, d->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? AR_OK
              : AR_ERR_CUDA;
@@ -946,9 +1037,162 @@ int ar_reduce_scatter_store(const void *const *partials, int n, int64_t count, i
   ra.ndst = world;
   ra.begin = begin;
   ra.end = end;
+  ra.status = d->status;
   return launch_reduce_flat(ra, n, d->sms, static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? AR_OK
              : AR_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------- cross-rank signals
+
+static int check_pads(void *const *pads, int world, int rank) {
+  if (world < 1 || world > AR_MAX_RANKS || rank < 0 || rank >= world || !pads) return AR_ERR_ARG;
+  for (int d = 0; d < world; ++d)
+    if (!pads[d]) return AR_ERR_ARG;
+  for (int d = 0; d < world; ++d)
+    if (!aligned16(pads[d])) return AR_ERR_ALIGN;
+  return AR_OK;
+}
+
+static int signal_call(void *const *pads, const void *mine, int world, int rank, uint32_t epoch,
+                       unsigned limit_us, bool post, bool wait, void *stream) {
+  if (wait && (limit_us == 0 || limit_us > 10000000u)) return AR_ERR_ARG;
+  int st;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  SignalArgs a;
+  std::memset(&a, 0, sizeof a);
+  if (post)
+    for (int k = 0; k < world; ++k) a.pads[k] = static_cast<uint32_t *>(pads[k]);
+  a.mine = static_cast<uint32_t *>(const_cast<void *>(mine));
+  a.world = world;
+  a.rank = rank;
+  a.post = post;
+  a.wait = wait;
+  a.epoch = epoch;
+  a.limit_ns = static_cast<uint64_t>(limit_us) * 1000u;
+  a.status = d->status;
+  return launch_signal(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+}
+
+int ar_signal_post(void *const *pads, int world, int rank, uint32_t epoch, void *stream) {
+  const int st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  return signal_call(pads, nullptr, world, rank, epoch, 0, true, false, stream);
+}
+
+int ar_signal_wait(const void *pad, int world, uint32_t epoch, unsigned limit_us, void *stream) {
+  if (!pad || world < 1 || world > AR_MAX_RANKS) return AR_ERR_ARG;
+  if (!aligned16(pad)) return AR_ERR_ALIGN;
+  return signal_call(nullptr, pad, world, 0, epoch, limit_us, false, true, stream);
+}
+
+int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned limit_us,
+               void *stream) {
+  const int st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  return signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+}
+
+int ar_selftest_barrier(int device, int world, int rounds, unsigned limit_us, int *mismatches) {
+  if (device < 0 || device >= kMaxDevices || world < 1 || world > AR_MAX_RANKS || rounds < 1 ||
+      rounds > 1000000 || limit_us == 0 || limit_us > 10000000u || !mismatches)
+    return AR_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  int st = AR_OK;
+  DeviceState *d = current_device(&st);
+  int *count = nullptr;
+  if (d) {
+    if (cudaMalloc(&count, sizeof(int)) != cudaSuccess || cudaMemset(count, 0, sizeof(int)) != cudaSuccess ||
+        launch_barrier_selftest(world, rounds, static_cast<uint64_t>(limit_us) * 1000u, d->status,
+                                count) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(mismatches, count, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      st = AR_ERR_CUDA;
+    }
+    if (count) cudaFree(count);
+  }
+  cudaSetDevice(prev);
+  if (st != AR_OK) return st;
+  return ar_device_status(device, 1);
+}
+
+int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, int rank, int world, void *const *temps,
+                        void *const *pads, uint32_t epoch, unsigned limit_us, void *stream) {
+  int st = check_shape(n, m, H, eps);
+  if (st != AR_OK) return st;
+  st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  if (limit_us == 0 || limit_us > 10000000u) return AR_ERR_ARG;
+  if (m == 0) return AR_OK;
+  if (!temps) return AR_ERR_ARG;
+  for (int e = 0; e < world; ++e)
+    if (!temps[e]) return AR_ERR_ARG;
+  for (int e = 0; e < world; ++e)
+    if (!aligned16(temps[e])) return AR_ERR_ALIGN;
+  st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, nullptr);
+  if (st != AR_OK) return st;
+  const int64_t bytes = m * H * 2;
+  for (int e = 0; e < world; ++e) {
+    const Range t = range_of(temps[e], bytes);
+    for (int k = 0; k < n; ++k)
+      if (overlap(t, range_of(partials[k], bytes))) return AR_ERR_ALIAS;
+    for (int f = e + 1; f < world; ++f)
+      if (overlap(t, range_of(temps[f], bytes))) return AR_ERR_ALIAS;
+  }
+  const Range mine = range_of(temps[rank], bytes);
+  if (overlap(mine, range_of(out, bytes)) || overlap(mine, range_of(residual_out, bytes)) ||
+      overlap(mine, range_of(residual, bytes)) || overlap(mine, range_of(weight, H * 2)))
+    return AR_ERR_ALIAS;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  ar_plan_t pl;
+  st = make_plan(n, m, H, AR_MODE_TWO_STAGE, d->sms, d->smem_optin, nullptr, &pl,
+                 device_register_occupancy);
+  if (st != AR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Stage 1: this rank's slice, stored into every rank's temporary.  The
+  // partials and temporaries of other ranks are peer mappings: no bulk
+  // prefetch there.
+  const int64_t npacks = m * H / kPackElems;
+  const int64_t per = (npacks + world - 1) / world;
+  const int64_t begin = static_cast<int64_t>(rank) * per;
+  const int64_t end = begin + per < npacks ? begin + per : npacks;
+  if (begin < end) {
+    ReduceArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
+    for (int e = 0; e < world; ++e) ra.dst[e] = static_cast<uint4 *>(temps[e]);
+    ra.ndst = world;
+    ra.prefetch = 0;
+    ra.begin = begin;
+    ra.end = end;
+    ra.status = d->status;
+    if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
+  }
+  // Every rank's stores into this rank's temporary have landed.
+  st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+  if (st != AR_OK) return st;
+  // Stage 2 on this rank's (local) temporary.
+  const void *temp_in[1] = {temps[rank]};
+  cudaError_t e;
+  if (pl.kernel == AR_KERNEL_STREAM) {
+    e = launch_stream(temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                      d->status, true, s);
+  } else {
+    EpilogueArgs a;
+    fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                       d->status);
+    e = launch_epilogue(a, 1, pl, true, s);
+  }
+  return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
 
 int ar_load_rmsnorm(const void *temp, const void *residual, const void *weight, float eps,
@@ -1034,6 +1278,7 @@ const char *ar_strerror(int status) {
     case AR_ERR_CUDA: return "CUDA runtime error or launch failure";
     case AR_ERR_TIMEOUT: return "a bounded device-side wait timed out";
     case AR_ERR_UNSUPPORTED: return "unsupported size (H above AR_MAX_HIDDEN or too many rows)";
+    case AR_ERR_BOUNDS: return "a device-side bounds check failed (checking build)";
     case AR_ERR_SCRATCH_LIMIT:
       return "m*H exceeds the fixed device scratch of ar_rmsnorm_two_stage_static (AR_STATIC_SCRATCH_ELEMS)";
     default: return "unknown status";

@@ -10,7 +10,31 @@
 
 #include "ar_rmsnorm.h"
 
+// The checking build (nvcc -DAR_CHECK=1, see _build.py) compiles device-side
+// bounds checks into the kernels: every index a kernel derives from its
+// launch shape (row, pack range, cluster rank, shared-memory slot, rank
+// count) is tested against the buffer or array it addresses before use.
+#ifndef AR_CHECK
+#define AR_CHECK 0
+#endif
+
 namespace arn {
+
+// `ok` in the checking build, where a false `ok` also records AR_ERR_BOUNDS
+// in the device status word; always true in the normal build (the test
+// compiles away).  The caller skips the access that `ok` guards: a thread
+// never leaves its kernel early, because the barriers of its CTA (or
+// cluster) would then wait for it forever.
+__device__ __forceinline__ bool in_bounds(bool ok, int *status) {
+#if AR_CHECK
+  if (!ok && status != nullptr) atomicExch(status, AR_ERR_BOUNDS);
+  return ok;
+#else
+  (void)ok;
+  (void)status;
+  return true;
+#endif
+}
 
 constexpr int kPackElems = 8;            // bf16 per 16-byte pack
 constexpr int kMaxClusterCtas = 16;      // widest row split (non-portable cluster)
@@ -31,6 +55,11 @@ struct EpilogueArgs {
   float eps;
   int early_reads;               // weight and residual may be read before the
                                  // wait on the previous grid (stage 2 only)
+  int prefetch_own;              // prefetch this CTA's slice of its row into L2
+                                 // before the wait on the previous grid
+  int64_t ahead;                 // > 0: after its sums, prefetch the same slice of
+                                 // row + ahead into L2 (the row the CTA that takes
+                                 // this one's place will read); 0: none
   uint64_t wait_limit_ns;        // bound of the cluster-exchange wait
   int *status;                   // device status word (AR_ERR_TIMEOUT on timeout)
 };
@@ -43,8 +72,10 @@ struct ReduceArgs {
   const uint4 *p[AR_MAX_RANKS];
   uint4 *dst[AR_MAX_RANKS];
   int ndst;
+  int prefetch;   // prefetch each CTA's first packs into L2 before the wait
   int64_t begin;
   int64_t end;
+  int *status;    // device status word (checking build: AR_ERR_BOUNDS)
 };
 
 // --- bf16 <-> fp32 ----------------------------------------------------------
@@ -78,6 +109,16 @@ __device__ __forceinline__ uint4 ld_ro(const uint4 *p) { return __ldg(p); }
 
 // Streaming 16-byte store: the outputs are not re-read by this kernel.
 __device__ __forceinline__ void st_stream(uint4 *p, const uint4 &v) { __stcs(p, v); }
+
+// Ask L2 to fetch `bytes` of global memory at `p` (both multiples of 16)
+// without waiting for it and without touching registers or L1
+// (cp.async.bulk.prefetch, the bulk-copy engine's prefetch form).  L2 is
+// the point of coherence of this GPU's memory, so a line prefetched before
+// another grid writes it is updated by that write: a prefetch may run
+// before griddepcontrol.wait.  Only for memory of this GPU.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 
 // --- reductions -----------------------------------------------------------------
 

@@ -72,6 +72,13 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   const int c1 = min(a.P, c0 + a.per_cta);
   const int64_t base = row * static_cast<int64_t>(a.P);
   const int T = blockDim.x;
+  // Checking build: the row exists, this CTA's pack range lies inside the
+  // row and its threads cover it, and the cluster rank addresses one of at
+  // most kMaxClusterCtas total slots.  Every access below is guarded by it.
+  const bool live = in_bounds(row < a.m && c0 >= 0 &&
+                                  (c1 <= c0 || (c1 <= a.P && c1 - c0 <= VPT * T)) &&
+                                  S <= static_cast<uint32_t>(kMaxClusterCtas) && q < S,
+                              a.status);
   if constexpr (CL) {
     if (threadIdx.x == 0) {
       mbar_init(&totals_bar, 1);
@@ -86,13 +93,24 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   // stage 2 the previous grid is stage 1, which writes neither the weight
   // nor the residual (and everything before stage 1 has completed), so
   // those two are read before the wait; the temporary only after.
+  //
+  // Before that wait, lanes 0..N of warp 0 ask L2 for this CTA's slice of
+  // the n partials and the residual, one bulk prefetch each.  Under
+  // programmatic dependent launch this grid's CTAs start while the previous
+  // grid still runs, so the DRAM round trip of the first loads overlaps its
+  // tail; the loads after the wait then find their lines in L2 (or in
+  // flight).  Nothing enters registers or L1 before the wait.
   float r[VPT][8];
   uint4 wv[VPT], rv[VPT];
+  if (live && a.prefetch_own && threadIdx.x <= N && c1 > c0) {
+    const uint4 *src = threadIdx.x < N ? a.p[threadIdx.x] : a.res;
+    prefetch_l2(src + base + c0, static_cast<uint32_t>(c1 - c0) * 16u);
+  }
   if (!a.early_reads) pdl_wait_prior_grid();
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
-    if (c < c1) {
+    if (live && c < c1) {
       if constexpr (!LW) wv[v] = ld_ro(a.w + c);
       rv[v] = ld_ro(a.res + base + c);
     }
@@ -102,7 +120,7 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
-    if (c < c1) {
+    if (live && c < c1) {
       float acc[8], rs[8];
       sum_pack_in_rank_order<N>(a.p, base + c, acc);
       unpack8(rv[v], rs);
@@ -119,12 +137,20 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
     }
   }
 
+  // The row one wave ahead: this CTA's loads have landed, so while it
+  // reduces and stores, L2 fetches the slice that the CTA taking its place
+  // (a later wave) will read.
+  if (live && a.ahead > 0 && threadIdx.x <= N && c1 > c0 && row + a.ahead < a.m) {
+    const uint4 *src = threadIdx.x < N ? a.p[threadIdx.x] : a.res;
+    prefetch_l2(src + base + a.ahead * a.P + c0, static_cast<uint32_t>(c1 - c0) * 16u);
+  }
+
   // residual_out = bf16(r); square sum of this thread's r.
   float ss = 0.f;
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
-    if (c < c1) st_stream(a.rout + base + c, pack8(r[v]));
+    if (live && c < c1) st_stream(a.rout + base + c, pack8(r[v]));
 #pragma unroll
     for (int e = 0; e < 8; ++e) ss = fmaf(r[v][e], r[v][e], ss);
   }
@@ -133,24 +159,25 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
 #pragma unroll
     for (int v = 0; v < VPT; ++v) {
       const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
-      if (c < c1) wv[v] = ld_ro(a.w + c);
+      if (live && c < c1) wv[v] = ld_ro(a.w + c);
     }
   }
   float total = block_sum(ss, red);
   if constexpr (CL) {
     cluster_wait_acquire();  // every peer runs and has initialised its barrier
     if (threadIdx.x == 0) mbar_arrive_expect_tx(&totals_bar, S * static_cast<uint32_t>(sizeof(float)));
-    if (threadIdx.x < S) st_async_remote_f32(&cta_totals[q], threadIdx.x, total, &totals_bar);
+    if (live && threadIdx.x < S) st_async_remote_f32(&cta_totals[q], threadIdx.x, total, &totals_bar);
     mbar_wait_bounded(&totals_bar, 0, &totals_abort, a.wait_limit_ns, a.status);
     total = 0.f;
-    for (uint32_t k = 0; k < S; ++k) total += cta_totals[k];
+    const uint32_t slots = AR_CHECK ? min(S, static_cast<uint32_t>(kMaxClusterCtas)) : S;
+    for (uint32_t k = 0; k < slots; ++k) total += cta_totals[k];
   }
   const float inv = rsqrtf(total / a.H + a.eps);
 
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
-    if (c < c1) {
+    if (live && c < c1) {
       float w[8], y[8];
       unpack8(wv[v], w);
 #pragma unroll

@@ -1,0 +1,267 @@
+// The cross-rank data plane of the all-reduce: the buffers of every rank
+// mapped into each rank's address space (CUDA IPC handles), and a bounded
+// flag barrier between the two stages of the two-stage path.
+//
+// ROCm/aiter #3817 "perf: optimize fused AllReduce + RMSNorm
+// (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: stage 1
+// of every rank stores its reduced slice straight into the temporary buffer
+// of every rank, so before stage 2 reads its own temporary every rank's
+// stores must have landed -- a cross-rank synchronisation the page implies
+// but does not describe.  lightseekorg/tokenspeed #968 "perf(comm): add
+// opt-in Triton AR+RMSNorm backend" maps the ranks' buffers with HIP IPC
+// handles and synchronises through signal flags; its review adds that a
+// rank which fails alone must not leave its peers waiting forever.  The
+// PyTorch symmetric-memory pages (pytorch #137643 stack) wait on a signal
+// pad in the same way.
+//
+// Here: every rank owns a signal pad of AR_MAX_RANKS 32-bit flags in its
+// own device memory, zeroed before first use.  Rank r "posts" epoch e by
+// storing e into flag r of every rank's pad (release, system scope, after a
+// system-scope fence that orders every write the previous grids made), and
+// "waits" for epoch e by spinning on every flag of its own pad until each
+// holds e or later (acquire, system scope).  Every wait is bounded by
+// %globaltimer: on timeout the kernel records AR_ERR_TIMEOUT in the device
+// status word and returns, so a missing peer becomes an error the host can
+// read rather than a hang.  No multicast or NVLS object is involved: plain
+// loads and stores through peer mappings.
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+
+#include "common.cuh"
+#include "peer.cuh"
+
+namespace arn {
+
+__device__ __forceinline__ void st_release_sys(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
+
+// Epoch e has been reached by a flag holding f when f - e, as a signed
+// 32-bit difference, is not negative (so epochs may wrap around).
+__device__ __forceinline__ bool reached(uint32_t f, uint32_t e) {
+  return static_cast<int32_t>(f - e) >= 0;
+}
+
+// Spin until *flag reaches epoch, for at most limit_ns; false on timeout.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t epoch, uint64_t limit_ns) {
+  if (reached(ld_acquire_sys(flag), epoch)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (reached(ld_acquire_sys(flag), epoch)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// One warp: lane d posts into rank d's pad, lane j waits for rank j's flag.
+__global__ void __launch_bounds__(32) k_signal(const __grid_constant__ SignalArgs a) {
+  // Everything the previous grids wrote (stage 1's stores into the peers'
+  // temporaries) is complete once this returns; the fence below makes it
+  // visible at system scope before the flag says so.
+  pdl_wait_prior_grid();
+  pdl_launch_dependents();
+  const int t = static_cast<int>(threadIdx.x);
+  // Checking build: a rank count the pad holds and a slot inside it.
+  if (!in_bounds(a.world >= 1 && a.world <= AR_MAX_RANKS && a.rank >= 0 && a.rank < a.world,
+                 a.status))
+    return;
+  if (a.post && t < a.world) {
+    fence_sys();
+    st_release_sys(a.pads[t] + a.rank, a.epoch);
+  }
+  if (a.wait && t < a.world && !wait_flag(a.mine + t, a.epoch, a.limit_ns))
+    atomicExch(a.status, AR_ERR_TIMEOUT);
+  __syncwarp();
+}
+
+cudaError_t launch_signal(const SignalArgs &a, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1, 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, k_signal, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- self-test
+//
+// All ranks of a barrier in one kernel: CTA r plays rank r.  A cooperative
+// launch guarantees that the `world` CTAs run at the same time (or the
+// launch fails), which ranks that wait on one another need.  Each round e,
+// rank r writes a value into its data slot of round parity e, posts epoch
+// e, waits for every rank, then reads every rank's slot of that parity: the
+// release/acquire pair must make each peer's value of round e visible.
+// (With two parities no rank can overwrite a slot before every rank has
+// read it: writing it again needs round e + 2, which needs every rank's
+// post of round e + 1, which each makes after its reads of round e.)
+
+static __device__ uint32_t g_selftest_pads[AR_MAX_RANKS * AR_MAX_RANKS];
+static __device__ uint32_t g_selftest_data[2 * AR_MAX_RANKS];
+
+__global__ void __launch_bounds__(32)
+k_barrier_selftest(int world, int rounds, uint64_t limit_ns, int *status, int *mismatches) {
+  const int rank = static_cast<int>(blockIdx.x);
+  const int t = static_cast<int>(threadIdx.x);
+  for (int e = 1; e <= rounds; ++e) {
+    const int parity = e & 1;
+    if (t == 0) g_selftest_data[parity * AR_MAX_RANKS + rank] = static_cast<uint32_t>(e * 1000 + rank);
+    __syncwarp();
+    if (t < world) {
+      fence_sys();
+      st_release_sys(g_selftest_pads + t * AR_MAX_RANKS + rank, static_cast<uint32_t>(e));
+    }
+    bool ok = true;
+    if (t < world) {
+      ok = wait_flag(g_selftest_pads + rank * AR_MAX_RANKS + t, static_cast<uint32_t>(e), limit_ns);
+      if (!ok) {
+        atomicExch(status, AR_ERR_TIMEOUT);
+      } else {
+        const uint32_t v = *reinterpret_cast<volatile uint32_t *>(
+            &g_selftest_data[parity * AR_MAX_RANKS + t]);
+        if (v != static_cast<uint32_t>(e * 1000 + t)) atomicAdd(mismatches, 1);
+      }
+    }
+    if (__any_sync(0xFFFFFFFFu, !ok)) return;  // a rank is missing: stop, do not wait again
+    __syncwarp();
+  }
+}
+
+cudaError_t launch_barrier_selftest(int world, int rounds, uint64_t limit_ns, int *status,
+                                    int *mismatches) {
+  void *pads = nullptr, *data = nullptr;
+  if (cudaGetSymbolAddress(&pads, g_selftest_pads) != cudaSuccess ||
+      cudaGetSymbolAddress(&data, g_selftest_data) != cudaSuccess)
+    return cudaGetLastError();
+  cudaError_t e = cudaMemset(pads, 0, sizeof(g_selftest_pads));
+  if (e == cudaSuccess) e = cudaMemset(data, 0, sizeof(g_selftest_data));
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(world), 1, 1);
+  cfg.blockDim = dim3(32, 1, 1);
+  cfg.stream = nullptr;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, k_barrier_selftest, world, rounds, limit_ns, status, mismatches);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- IPC handles
+
+namespace {
+
+// cuMemGetAddressRange, looked up from the driver at run time (the library
+// links only the runtime): the start of the allocation holding a pointer,
+// since an IPC handle names a whole allocation.
+using AddressRangeFn = int (*)(unsigned long long *base, size_t *size, unsigned long long ptr);
+
+AddressRangeFn address_range_fn() {
+  static std::once_flag once;
+  static AddressRangeFn fn = nullptr;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuMemGetAddressRange", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<AddressRangeFn>(p);
+    else
+      cudaGetLastError();
+  });
+  return fn;
+}
+
+// Allocations of other processes opened in this one, by handle: a handle
+// may be opened once per process, so repeated opens share the mapping.
+struct Opened {
+  void *base;
+  int refs;
+};
+std::mutex g_ipc_mu;
+std::map<std::string, Opened> g_opened;
+
+std::string key_of(const void *handle) {
+  return std::string(static_cast<const char *>(handle), sizeof(cudaIpcMemHandle_t));
+}
+
+}  // namespace
+}  // namespace arn
+
+using namespace arn;
+
+extern "C" {
+
+int ar_ipc_get_handle(const void *ptr, void *handle, int64_t *offset) {
+  if (!ptr || !handle || !offset) return AR_ERR_ARG;
+  const AddressRangeFn range = address_range_fn();
+  if (!range) return AR_ERR_CUDA;
+  unsigned long long base = 0;
+  size_t size = 0;
+  if (range(&base, &size, reinterpret_cast<unsigned long long>(ptr)) != 0 || base == 0)
+    return AR_ERR_ARG;  // not device memory of this process
+  cudaIpcMemHandle_t h;
+  if (cudaIpcGetMemHandle(&h, reinterpret_cast<void *>(base)) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  std::memcpy(handle, &h, sizeof h);
+  *offset = static_cast<int64_t>(reinterpret_cast<unsigned long long>(ptr) - base);
+  return AR_OK;
+}
+
+int ar_ipc_open(const void *handle, int64_t offset, void **ptr) {
+  if (!handle || !ptr || offset < 0) return AR_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_ipc_mu);
+  const std::string key = key_of(handle);
+  auto it = g_opened.find(key);
+  if (it == g_opened.end()) {
+    cudaIpcMemHandle_t h;
+    std::memcpy(&h, handle, sizeof h);
+    void *base = nullptr;
+    if (cudaIpcOpenMemHandle(&base, h, cudaIpcMemLazyEnablePeerAccess) != cudaSuccess) {
+      cudaGetLastError();
+      return AR_ERR_CUDA;
+    }
+    it = g_opened.emplace(key, Opened{base, 0}).first;
+  }
+  ++it->second.refs;
+  *ptr = static_cast<char *>(it->second.base) + offset;
+  return AR_OK;
+}
+
+int ar_ipc_close(const void *handle) {
+  if (!handle) return AR_ERR_ARG;
+  std::lock_guard<std::mutex> lock(g_ipc_mu);
+  auto it = g_opened.find(key_of(handle));
+  if (it == g_opened.end()) return AR_ERR_ARG;
+  if (--it->second.refs > 0) return AR_OK;
+  const cudaError_t e = cudaIpcCloseMemHandle(it->second.base);
+  g_opened.erase(it);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  return AR_OK;
+}
+
+}  // extern "C"

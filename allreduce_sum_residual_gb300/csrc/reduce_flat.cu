@@ -26,11 +26,25 @@ __global__ void __launch_bounds__(kReduceThreads)
 k_reduce_flat(const __grid_constant__ ReduceArgs a) {
   // Previous grids first, then let stage 2 be scheduled; stage 2 waits for
   // this grid's results itself (griddepcontrol.wait) before reading them.
+  // Before the wait, one thread per partial asks L2 for the CTA's first
+  // step of packs (a bulk prefetch), so that the first DRAM round trip
+  // overlaps the previous grid's tail.
+  // Checking build: a valid destination count and pack range.
+  const bool live = in_bounds(a.ndst >= 1 && a.ndst <= AR_MAX_RANKS && a.begin >= 0 &&
+                                  a.begin <= a.end,
+                              a.status);
+  if (live && a.prefetch && threadIdx.x < N) {
+    const int64_t b0 = a.begin + static_cast<int64_t>(blockIdx.x) * kReduceThreads * U;
+    if (b0 < a.end) {
+      const int64_t cnt = a.end - b0 < kReduceThreads * U ? a.end - b0 : kReduceThreads * U;
+      prefetch_l2(a.p[threadIdx.x] + b0, static_cast<uint32_t>(cnt) * 16u);
+    }
+  }
   pdl_wait_prior_grid();
   pdl_launch_dependents();
   const int64_t stride = static_cast<int64_t>(gridDim.x) * kReduceThreads * U;
   for (int64_t i0 = a.begin + static_cast<int64_t>(blockIdx.x) * kReduceThreads * U + threadIdx.x;
-       i0 < a.end; i0 += stride) {
+       live && i0 < a.end; i0 += stride) {
     float acc[U][8];
 #pragma unroll
     for (int u = 0; u < U; ++u) {

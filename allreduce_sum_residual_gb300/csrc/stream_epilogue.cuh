@@ -46,6 +46,11 @@ struct StreamArgs {
   float eps;
   uint64_t wait_limit_ns;              // bound of every mbarrier wait
   int *status;                         // device status word (AR_ERR_TIMEOUT on timeout)
+  int prefetch_first;                  // L2 prefetch of the CTA's first row before
+                                       // the wait on the previous grid
+  int prefetch_next;                   // L2 prefetch of the CTA's next row while it
+                                       // streams the current one
+  int smem_bytes;                      // dynamic shared memory of the launch
 };
 
 // --- bulk copy (PTX) -----------------------------------------------------------
@@ -86,7 +91,16 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int C = Tc >> 5;
-  if (threadIdx.x == 0) {
+  // Checking build: the ring, its barriers and the reduction scratch fit
+  // the launch's shared memory, the consumers are whole warps (at most
+  // kStreamMaxConsumers, one scratch slot each), and the row's tiles fit
+  // the template's VPT.  When this fails nothing below touches memory.
+  const bool live = in_bounds(
+      Tc >= 32 && Tc % 32 == 0 && Tc <= kStreamMaxConsumers && S >= 1 && a.tiles >= 1 &&
+          a.tiles <= VPT && static_cast<int64_t>(a.tiles) * Tc >= a.P &&
+          static_cast<int64_t>(S) * slot_packs * 16 + 16 * S + 64 * 4 + 4 <= a.smem_bytes,
+      a.status);
+  if (live && threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], C);
@@ -95,16 +109,28 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  pdl_wait_prior_grid();
-
   const int64_t G = gridDim.x;
   const int V = a.tiles;
+  // Before the wait: lanes 0..N of the producer warp ask L2 for this CTA's
+  // first row of every input.  A CTA that starts while the previous grid's
+  // last CTAs still run (on an SM they left) overlaps its first DRAM round
+  // trip with their tail.
+  if (live && a.prefetch_first && warp == 0 && lane <= N && blockIdx.x < a.m)
+    prefetch_l2(a.src[lane] + static_cast<int64_t>(blockIdx.x) * a.P,
+                static_cast<uint32_t>(a.P) * 16u);
+  pdl_wait_prior_grid();
 
   if (warp == 0) {
     // ---------------- producer
-    if (lane != 0) return;
+    if (lane != 0 || !live) return;
     int64_t t = 0;
     for (int64_t row = blockIdx.x; row < a.m; row += G) {
+      // The next row of this CTA, one row ahead of the ring's copies.
+      if (a.prefetch_next && row + G < a.m) {
+#pragma unroll 1
+        for (int j = 0; j <= N; ++j)
+          prefetch_l2(a.src[j] + (row + G) * a.P, static_cast<uint32_t>(a.P) * 16u);
+      }
       for (int v = 0; v < V; ++v, ++t) {
         const int s = static_cast<int>(t % S);
         const int64_t k = t / S;
@@ -147,12 +173,12 @@ k_stream_epilogue(const __grid_constant__ StreamArgs a) {
 #pragma unroll
   for (int v = 0; v < kWRegs; ++v) {
     const int c = v * Tc + tc;
-    wv[v] = (VPT <= 4 && v < V && c < a.P) ? ld_ro(a.w + c) : make_uint4(0, 0, 0, 0);
+    wv[v] = (live && VPT <= 4 && v < V && c < a.P) ? ld_ro(a.w + c) : make_uint4(0, 0, 0, 0);
   }
 
   int64_t t = 0;
   int parity_row = 0;
-  for (int64_t row = blockIdx.x; row < a.m; row += G, parity_row ^= 1) {
+  for (int64_t row = blockIdx.x; live && row < a.m; row += G, parity_row ^= 1) {
     const int64_t base = row * a.P;
     if (row + G >= a.m) pdl_launch_dependents();  // last row of this CTA
     float r[VPT][8];

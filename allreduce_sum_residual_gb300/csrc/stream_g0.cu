@@ -35,3 +35,16 @@ cudaError_t launch_bounded_wait_selftest(uint64_t limit_ns, int *status, cudaStr
 }
 
 }  // namespace arn
+
+namespace arn {
+
+// One failing bounds check and nothing else: in the checking build it
+// records AR_ERR_BOUNDS, in the normal build the check compiles away.
+__global__ void k_bounds_selftest(int *status) { (void)in_bounds(false, status); }
+
+cudaError_t launch_bounds_selftest(int *status, cudaStream_t s) {
+  k_bounds_selftest<<<1, 1, 0, s>>>(status);
+  return cudaGetLastError();
+}
+
+}  // namespace arn

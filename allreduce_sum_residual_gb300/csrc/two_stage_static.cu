@@ -15,6 +15,7 @@ namespace arn {
 int two_stage_with_temp(const void *const *partials, int n, const void *residual,
                         const void *weight, float eps, int64_t m, int64_t H, void *out,
                         void *residual_out, void *temp, int64_t temp_elems, void *stream);
+int check_call_shape(int n, int64_t m, int64_t H, float eps);
 
 namespace {
 
@@ -51,7 +52,11 @@ extern "C" int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
                                            const void *residual, const void *weight, float eps,
                                            int64_t m, int64_t H, void *out, void *residual_out,
                                            void *stream) {
-  if (n < 1 || n > AR_MAX_RANKS || m < 0 || H <= 0) return AR_ERR_ARG;
+  // The same shape checks, in the same order, as every other entry point
+  // (n, m, H, eps; then H's alignment and AR_MAX_HIDDEN); then this entry
+  // point's own limit; only then is m == 0 a no-op.
+  const int shape = arn::check_call_shape(n, m, H, eps);
+  if (shape != AR_OK) return shape;
   if (m > AR_STATIC_SCRATCH_ELEMS / H) return AR_ERR_SCRATCH_LIMIT;
   if (m == 0) return AR_OK;
   void *scratch = nullptr;

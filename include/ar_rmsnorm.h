@@ -78,6 +78,9 @@ extern "C" {
 #define AR_ERR_UNSUPPORTED 7  /* H above AR_MAX_HIDDEN                         */
 #define AR_ERR_SCRATCH_LIMIT 8 /* m*H above AR_STATIC_SCRATCH_ELEMS
                                   (ar_rmsnorm_two_stage_static only)          */
+#define AR_ERR_BOUNDS      9  /* a device-side bounds check failed (only the
+                                 checking build, compiled with AR_CHECK=1,
+                                 has these checks; the access was skipped)    */
 
 /* Modes. */
 #define AR_MODE_AUTO       0  /* pick by ar_select_mode(n, m, H)               */
@@ -89,7 +92,10 @@ extern "C" {
 #define AR_STREAM_MAX_HIDDEN 32768 /* largest H of the stream kernel           */
 
 /*
- * The fused epilogue.
+ * The fused epilogue: the all-reduce of the n rank partials, the residual
+ * add and RMSNorm in one call (ROCm/aiter #3817 "perf: optimize fused
+ * AllReduce + RMSNorm (custom_all_reduce)", Motivation and Technical
+ * Details: the one-stage and two-stage paths).
  *   partials     host array of n device pointers, each [m, H] bf16; index
  *                order is the reduce order.
  *   n            number of partials (ranks), 1 .. AR_MAX_RANKS.
@@ -122,7 +128,24 @@ typedef struct {
   int stages;      /* stream kernel: shared-memory ring slots; else 0         */
   int64_t ctas;    /* CTAs of the epilogue kernel                              */
   int launches;    /* kernels one call launches (1 or 2)                      */
+  int prefetch;    /* L2 prefetch of the epilogue kernel: AR_PREFETCH_NONE,
+                      AR_PREFETCH_ROW or AR_PREFETCH_ROW_AHEAD                */
 } ar_plan_t;
+
+/* L2 prefetch (ar_plan_t.prefetch).  A prefetch only asks L2 to fetch
+   lines of this GPU's memory; it changes no result. */
+#define AR_PREFETCH_AUTO      0  /* library's choice (forcing only)            */
+#define AR_PREFETCH_NONE      1
+#define AR_PREFETCH_ROW       2  /* each CTA prefetches its own (first) row
+                                    slice of the inputs before it waits for
+                                    the previous grid in the stream (one-
+                                    stage; two-stage prefetches in stage 1
+                                    instead)                                */
+#define AR_PREFETCH_ROW_AHEAD 3  /* as ROW, and: register kernel (one CTA per
+                                    row only): after its sums each CTA
+                                    prefetches the slice of the row one wave
+                                    of CTAs ahead; stream kernel: the
+                                    producer prefetches the CTA's next row */
 
 /* Epilogue kernels (ar_plan_t.kernel). */
 #define AR_KERNEL_AUTO      0  /* library's choice (forcing only)             */
@@ -138,7 +161,9 @@ typedef struct {
 
 /*
  * The plan ar_rmsnorm would follow for (n, m, H, mode) on a GPU with
- * `sm_count` SMs (0: ask the current device).  Pure host logic when
+ * `sm_count` SMs (0: ask the current device): the path the selection rule
+ * picks (ROCm/aiter #3817, Test Results: the one-/two-stage thresholds)
+ * and the launch shape of its kernels.  Pure host logic when
  * sm_count > 0: the measured plan table with plain interpolation between
  * its rows columns.  With sm_count = 0 it is exactly ar_rmsnorm's plan on
  * the current device, whose interpolation also uses each kernel's occupancy
@@ -161,13 +186,20 @@ typedef int (*ar_occupancy_fn)(int inputs, int vpt, int late_weight, int threads
  * table that ar_rmsnorm does with the device's own figures: plan for
  * another GPU, or test the planner.  ctas_per_sm may be NULL (plain
  * interpolation).  It is called during the call only.  AR_ERR_ARG for
- * sm_count <= 0 or a NULL plan.
+ * sm_count <= 0 or a NULL plan.  Library utility (no passage of the pages
+ * defines it).
  */
 int ar_get_plan_ex(int n, int64_t m, int64_t H, int mode, int sm_count,
                    ar_occupancy_fn ctas_per_sm, ar_plan_t *plan);
 
 /*
- * As ar_rmsnorm, with two additions for testing and tuning:
+ * As ar_rmsnorm, with two additions for testing and tuning.  The reduced sum
+ * is exposed because the pages make its bit-exactness the contract: the
+ * sum follows the order of the rank pointers, so it stays bit-identical
+ * whatever the kernel (ROCm/aiter #3817, Technical Details, 2stage,
+ * reduce-scatter).  The forced plan plays the role of the page's switch
+ * that pins the one- or two-stage path for benchmarking (AITER_AR_1STAGE,
+ * same page, Test Plan), extended to the kernel and its launch shape.
  *   sum_out  [m, H] fp32 device buffer (16-byte aligned) that receives the
  *            reduced sum feeding the residual add: the fp32 accumulator for
  *            one-stage, the widened bf16 temporary for two-stage.  NULL to
@@ -194,10 +226,13 @@ int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
 
 /*
  * As ar_rmsnorm, but any of the partials, residual, weight, out and
- * residual_out may live in host memory that is pinned and mapped into the
- * device's address space (cudaHostAlloc / cudaMallocHost, or
- * cudaHostRegister, under unified addressing: the device address equals the
- * host address).  The kernels read and write such buffers directly over the
+ * residual_out may live outside this process's own device memory: in host
+ * memory that is pinned and mapped into the device's address space
+ * (cudaHostAlloc / cudaMallocHost, or cudaHostRegister, under unified
+ * addressing: the device address equals the host address), in another
+ * process's allocation opened with ar_ipc_open (the one-shot all-reduce:
+ * every rank reads every rank's partial), or in another GPU's memory that
+ * this device can reach (peer access).  The kernels read and write such buffers directly over the
  * host link (NVLink-C2C on Grace systems): no staging copy, no device memory
  * beyond the two-stage workspace.  The epilogue runs on the register kernel
  * (plain 16-byte loads and stores).  Results are bit-identical to
@@ -205,8 +240,11 @@ int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
  *
  * Each pointer is checked with cudaPointerGetAttributes before anything is
  * launched: it must be device memory of the current device, managed
- * memory, or mapped pinned host memory; anything else (pageable host
- * memory, another device's memory) returns AR_ERR_ARG.  As everywhere in
+ * memory, mapped pinned host memory, or memory of a GPU this device has
+ * peer access to; anything else (pageable host memory, a device without
+ * peer access) returns AR_ERR_ARG.  The pages have no
+ * host-buffer path: this entry point has no counterpart there; what it
+ * computes is ar_rmsnorm's.  As everywhere in
  * this library, each buffer must hold the bytes its shape implies.  The
  * host memory must stay pinned and untouched by the host until the stream
  * has passed the call.  The checks cost a few microseconds per call.
@@ -294,10 +332,114 @@ int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
                                 float eps, int64_t m, int64_t H, void *out,
                                 void *residual_out, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Cross-rank data plane: what the all-reduce needs when the n partials are
+ * the buffers of n processes (one per GPU, or several on one GPU).
+ *
+ * ROCm/aiter #3817, Technical Details, 2stage, reduce-scatter: each rank
+ * reduces its slice of the packs across every rank's partial and stores the
+ * bf16 sums straight into every rank's temporary, so every rank's stores
+ * must have landed before any rank's stage 2 reads its own temporary.
+ * lightseekorg/tokenspeed #968, Summary: the ranks' buffers are mapped into
+ * each other's address spaces through IPC handles, with a collective
+ * fallback when that setup fails on any rank.
+ *
+ * Signal pads: each rank owns a pad of AR_MAX_RANKS 32-bit flags in its own
+ * device memory (16-byte aligned, zeroed before first use).  Rank r posts
+ * epoch e by storing e into flag r of every rank's pad (a system-scope fence
+ * orders the writes of all previous grids on the stream before it, then a
+ * release store); it waits for epoch e by spinning on its own pad until
+ * every one of the first `world` flags holds e or later (acquire; a flag f
+ * has reached e when (int32_t)(f - e) >= 0, so epochs may wrap).  Use a new
+ * epoch for every barrier.  A wait gives up after limit_us microseconds
+ * (1 .. 10^7), records AR_ERR_TIMEOUT in the device status word
+ * (ar_device_status) and returns: a rank that never arrives is an error, not
+ * a hang.  Kernels of different ranks that wait on one another must run at
+ * the same time, so never run several ranks' waits as separate launches on
+ * one GPU (in one or several processes): order such ranks on the host.
+ * --------------------------------------------------------------------------- */
+
+#define AR_SIGNAL_PAD_BYTES (AR_MAX_RANKS * 4)
+#define AR_IPC_HANDLE_BYTES 64
+
+/* Post epoch `epoch` of rank `rank` into flag `rank` of pads[0 .. world-1]
+   (rank order; other ranks' pads through peer or IPC mappings).  The
+   cross-rank sync of aiter #3817's 2stage path (section note above). */
+int ar_signal_post(void *const *pads, int world, int rank, uint32_t epoch, void *stream);
+
+/* Wait until flags 0 .. world-1 of this rank's `pad` reach `epoch` (the
+   same passages as ar_signal_post). */
+int ar_signal_wait(const void *pad, int world, uint32_t epoch, unsigned limit_us, void *stream);
+
+/* Post, then wait on pads[rank]: a barrier of the `world` ranks (the same
+   passages as ar_signal_post). */
+int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned limit_us,
+               void *stream);
+
+/*
+ * Two-stage epilogue of rank `rank` of `world` ranks, all on `stream`:
+ * stage 1 reduces this rank's slice of the packs (as ar_reduce_scatter_store)
+ * across the n partials and stores it into every rank's temporary
+ * temps[0 .. world-1]; ar_barrier(pads, world, rank, epoch, limit_us); then
+ * stage 2 (residual add and RMSNorm) on temps[rank], this rank's own.  The
+ * results equal ar_rmsnorm's two-stage results once every rank has run it
+ * with the same epoch (ROCm/aiter #3817, Technical Details, 2stage, across
+ * processes).  partials[k] and temps[d] of other ranks are peer or
+ * IPC mappings; temps[rank], residual, weight, out and residual_out are this
+ * device's memory.  Arguments otherwise as ar_rmsnorm and
+ * ar_reduce_scatter_store; no temp may overlap a partial, another temp or an
+ * output (AR_ERR_ALIAS).
+ */
+int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, int rank, int world, void *const *temps,
+                        void *const *pads, uint32_t epoch, unsigned limit_us, void *stream);
+
+/*
+ * CUDA IPC handle (AR_IPC_HANDLE_BYTES bytes into `handle`) of the
+ * allocation holding the device pointer `ptr`, and ptr's byte offset in it
+ * (an IPC handle names a whole allocation).  Send both to the other ranks.
+ * AR_ERR_ARG when ptr is not device memory of this process.  The setup of
+ * tokenspeed #968's IPC path (Summary), in this library's C ABI.
+ */
+int ar_ipc_get_handle(const void *ptr, void *handle, int64_t *offset);
+
+/*
+ * Map another process's allocation (its handle from ar_ipc_get_handle) into
+ * this one and return the address of byte `offset` in it (tokenspeed #968's
+ * IPC setup, as ar_ipc_get_handle).  Opening the same
+ * handle again returns the same mapping (reference counted).  AR_ERR_CUDA
+ * when the runtime refuses (for example a handle of this very process).
+ */
+int ar_ipc_open(const void *handle, int64_t offset, void **ptr);
+
+/* Drop one reference to a mapping made by ar_ipc_open (the same passages);
+   the last one unmaps it.  AR_ERR_ARG for a handle that is not open. */
+int ar_ipc_close(const void *handle);
+
+/*
+ * Run a barrier of `world` ranks for `rounds` rounds inside one cooperative
+ * kernel on `device` (block r plays rank r, so the ranks run at the same
+ * time), each round checking that every rank's data written before its post
+ * is visible after the wait.  *mismatches receives the number of stale
+ * reads (0 expected); returns the status word after the run (AR_OK
+ * expected; AR_ERR_TIMEOUT if a wait ran out), then clears it.  Library
+ * utility (no passage of the pages defines it).
+ */
+int ar_selftest_barrier(int device, int world, int rounds, unsigned limit_us, int *mismatches);
+
 /*
  * Reserve the two-stage workspace (max_elems bf16 elements, i.e. the largest
- * m*H the two-stage path will see) on `device`.  Allocates with cudaMalloc,
- * so call it before any graph capture.  Growing replaces the old buffer
+ * m*H the two-stage path will see) on `device`: the temporary buffer stage
+ * 1 writes and stage 2 reads (ROCm/aiter #3817, Technical Details, 2stage,
+ * reduce-scatter).  It is a call of its own, made once before any capture,
+ * because setup inside a CUDA-graph capture breaks the capture, and a call
+ * that cannot get its workspace must fail the same way every time instead
+ * of retrying the setup (lightseekorg/tokenspeed #968, review of the state
+ * creation: a failed setup must be remembered as a permanent decline).
+ * The two-stage path never allocates: without a large enough workspace it
+ * returns AR_ERR_WORKSPACE.  Allocates with cudaMalloc, so call it before
+ * any graph capture.  Growing replaces the old buffer
  * (after a device synchronisation); a smaller request keeps the current one.
  * All two-stage calls on a device share this one buffer: two-stage calls
  * that may overlap on the GPU (different streams without ordering between
@@ -306,25 +448,37 @@ int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
  */
 int ar_reserve_workspace(int64_t max_elems, int device);
 
-/* Free the workspace of `device` (synchronises the device first). */
+/*
+ * Free the workspace of `device` (synchronises the device first).  The
+ * counterpart of ar_reserve_workspace (same passages): the buffer's
+ * lifetime is the caller's decision, never a side effect of a call.
+ */
 int ar_release_workspace(int device);
 
-/* Elements (bf16) of workspace currently reserved on `device`, or -1. */
+/* Elements (bf16) of workspace currently reserved on `device`, or -1.
+   Library utility (no passage of the pages defines it). */
 int64_t ar_workspace_elems(int device);
 
 /*
  * The mode AR_MODE_AUTO picks for (n, m, H): AR_MODE_ONE_STAGE or
- * AR_MODE_TWO_STAGE, from a threshold table measured on GB300 (the pages'
- * own rule, one-stage for m <= 32 at 4 ranks and m <= 16 at 8, was set on
- * MI355X: ROCm/aiter #3817, Test Results).  Pure host logic; needs no GPU.
- * Returns -AR_ERR_ARG for n outside [1, AR_MAX_RANKS], m < 0 or H <= 0.
+ * AR_MODE_TWO_STAGE.  The pages' rule, one-stage for m <= 32 at 4 ranks
+ * and m <= 16 at 8, was set on MI355X across GPUs (ROCm/aiter #3817, Test
+ * Results).  On one GB300 the measured sweep (n in {4, 8}, H in {4096,
+ * 8192}, m = 1 .. 16384) found one-stage faster at every shape, so the
+ * threshold is unbounded: this returns AR_MODE_ONE_STAGE for every valid
+ * (n, m, H), and n and H do not change the answer today.  Pure host logic;
+ * needs no GPU.  Returns -AR_ERR_ARG for n outside [1, AR_MAX_RANKS], m < 0
+ * or H <= 0.
  */
 int ar_select_mode(int n, int64_t m, int64_t H);
 
 /*
  * The device status word of `device`: AR_OK, or AR_ERR_TIMEOUT once a
  * bounded wait inside a kernel gave up (the kernel then stops early and its
- * outputs are not valid).  Synchronises the device; `reset` != 0 clears the
+ * outputs are not valid).  Waits are bounded because a peer that never
+ * arrives must turn into an error, not a hang (lightseekorg/tokenspeed
+ * #968, review of the state creation: one rank failing alone left the
+ * others in barriers that could hang the process group).  Synchronises the device; `reset` != 0 clears the
  * word.  Not for use inside graph capture.
  */
 int ar_device_status(int device, int reset);
@@ -334,13 +488,33 @@ int ar_device_status(int device, int reset);
  * that nothing completes, bounded by limit_us microseconds, and return what
  * the status word then holds (AR_ERR_TIMEOUT expected) after clearing it.
  * Checks the bounded-wait path without faulting or hanging the GPU.
+ * Library utility (no passage of the pages defines it).
  */
 int ar_selftest_bounded_wait(int device, unsigned limit_us);
 
-/* A short English description of a status code (static storage). */
+/*
+ * 1 in the checking build (compiled with AR_CHECK=1: every kernel tests the
+ * indices it derives from its launch shape before use, records
+ * AR_ERR_BOUNDS in the status word and skips the access when one fails),
+ * 0 in the normal build.  Library utility (no passage of the pages defines
+ * it).
+ */
+int ar_checks_bounds(void);
+
+/*
+ * Launch, on `device`, a kernel whose only work is one failing bounds check
+ * and return the status word after it (AR_ERR_BOUNDS in the checking build,
+ * AR_OK in the normal build, where the check compiles away), then clear
+ * it.  Library utility (no passage of the pages defines it).
+ */
+int ar_selftest_bounds(int device);
+
+/* A short English description of a status code (static storage).
+   Library utility (no passage of the pages defines it). */
 const char *ar_strerror(int status);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch.
+   Library utility (no passage of the pages defines it). */
 int ar_version(void);
 
 #ifdef __cplusplus

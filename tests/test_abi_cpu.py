@@ -31,6 +31,30 @@ def test_header_declares_the_boundary():
         assert must in names
 
 
+def declaration_comments():
+    """{function: the comment block right before its declaration}."""
+    out = {}
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        for m in re.finditer(r"/\*(?:(?!\*/).)*\*/\s*(?:#define[^\n]*\n\s*)*"
+                             r"[A-Za-z_][\w\s\*]*?\b(ar_\w+)\s*\(", src, flags=re.S):
+            block = m.group(0)
+            out[m.group(1)] = block[block.rfind("/*"):block.find("*/", block.rfind("/*")) + 2]
+    return out
+
+
+def test_every_declaration_cites_a_passage_or_says_it_has_none():
+    """Each entry point's comment names the page that defines what it does
+    (the page's PR number), or says that no passage of the pages defines it."""
+    comments = declaration_comments()
+    assert set(comments) == set(declared_functions())
+    missing = [name for name, text in comments.items()
+               if not any(k in " ".join(text.replace("*", " ").split()) for k in (
+                   "#3817", "#968", "#137643", "same passages", "Library utility",
+                   "no counterpart"))]
+    assert not missing, missing
+
+
 def test_library_exports_every_declared_symbol(arlib):
     so = ctypes.CDLL(arlib.LIB_PATH)
     missing = [n for n in declared_functions() if not hasattr(so, n)]
@@ -121,6 +145,78 @@ def test_stage_entry_points_check_arguments(arlib):
                              BASE + 16384, None) == ARG
 
 
+def test_static_scratch_entry_point_checks_shape_first(arlib):
+    """ar_rmsnorm_two_stage_static runs ar_rmsnorm's shape checks in the same
+    order before its own size limit, and only then treats m == 0 as a no-op
+    (all of it before any CUDA call)."""
+    L = arlib.lib()
+    arr = (ctypes.c_void_p * 2)(BASE, BASE + (1 << 20))
+    SCRATCH_LIMIT = 8
+    limit = arlib.AR_STATIC_SCRATCH_ELEMS
+
+    def call(n=2, m=4, H=1024, eps=1e-6):
+        return L.ar_rmsnorm_two_stage_static(arr, n, None, None, eps, m, H, None, None, None)
+
+    assert call(m=0, eps=float("nan")) == ARG
+    assert call(m=0, eps=-1.0) == ARG
+    assert call(m=0, H=1020) == ALIGN
+    assert call(m=0, H=arlib.AR_MAX_HIDDEN + 8) == UNSUPPORTED
+    assert call(m=0, n=0) == ARG and call(m=-1) == ARG and call(H=0) == ARG
+    assert call(m=limit // 1024 + 1, H=1020) == ALIGN              # alignment before the limit
+    assert call(m=limit // 8192 + 1, H=8192) == SCRATCH_LIMIT
+    assert call(m=limit // 8192 + 1, H=8192, eps=float("inf")) == ARG
+    assert call(m=0) == OK                                         # no pointers needed
+    # ar_rmsnorm gives the same codes for the same shape errors
+    for kw in (dict(m=0, eps=float("nan")), dict(m=0, H=1020), dict(m=0, H=arlib.AR_MAX_HIDDEN + 8)):
+        a = {**dict(n=2, m=4, H=1024, eps=1e-6), **kw}
+        assert L.ar_rmsnorm(arr, a["n"], None, None, a["eps"], a["m"], a["H"], None, None, 2,
+                            None) == call(**a)
+
+
+def test_cross_rank_calls_check_arguments_first(arlib):
+    """The signal, barrier, two-shot and IPC calls refuse bad arguments
+    before any CUDA call."""
+    L = arlib.lib()
+    pads = (ctypes.c_void_p * 2)(BASE, BASE + 4096)
+    assert L.ar_signal_post(pads, 0, 0, 1, None) == ARG          # world
+    assert L.ar_signal_post(pads, 2, 2, 1, None) == ARG          # rank >= world
+    assert L.ar_signal_post(pads, 17, 0, 1, None) == ARG
+    assert L.ar_signal_post(None, 2, 0, 1, None) == ARG
+    assert L.ar_signal_post((ctypes.c_void_p * 2)(BASE, 0), 2, 0, 1, None) == ARG
+    assert L.ar_signal_post((ctypes.c_void_p * 2)(BASE, BASE + 4), 2, 0, 1, None) == ALIGN
+    assert L.ar_signal_wait(None, 2, 1, 1000, None) == ARG
+    assert L.ar_signal_wait(BASE + 4, 2, 1, 1000, None) == ALIGN
+    assert L.ar_signal_wait(BASE, 2, 1, 0, None) == ARG          # unbounded wait refused
+    assert L.ar_signal_wait(BASE, 2, 1, 10_000_001, None) == ARG
+    assert L.ar_barrier(pads, 2, 0, 1, 0, None) == ARG
+    assert L.ar_barrier(pads, 2, -1, 1, 1000, None) == ARG
+    temps = (ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (12 << 20))
+    parts = (ctypes.c_void_p * 2)(BASE + (16 << 20), BASE + (20 << 20))
+    two_shot = lambda **k: L.ar_rmsnorm_two_shot(
+        parts, 2, BASE + (24 << 20), BASE + (28 << 20), k.get("eps", 1e-6), k.get("m", 4),
+        k.get("H", 1024), BASE + (32 << 20), BASE + (36 << 20), k.get("rank", 0),
+        k.get("world", 2), k.get("temps", temps), k.get("pads", pads), 1, k.get("limit", 1000), None)
+    assert two_shot(m=0) == OK                                     # checks only the sizes
+    assert two_shot(eps=-1.0) == ARG and two_shot(H=1020) == ALIGN
+    assert two_shot(rank=2) == ARG and two_shot(limit=0) == ARG
+    assert two_shot(temps=(ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (8 << 20) + 8)) == ALIGN
+    assert two_shot(temps=(ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (8 << 20) + 16)) == ALIAS
+    assert two_shot(temps=(ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (16 << 20))) == ALIAS
+    h = ctypes.create_string_buffer(64)
+    off = ctypes.c_int64(0)
+    assert L.ar_ipc_get_handle(None, h, ctypes.byref(off)) == ARG
+    assert L.ar_ipc_get_handle(BASE, None, ctypes.byref(off)) == ARG
+    p = ctypes.c_void_p()
+    assert L.ar_ipc_open(None, 0, ctypes.byref(p)) == ARG
+    assert L.ar_ipc_open(h, -1, ctypes.byref(p)) == ARG
+    assert L.ar_ipc_close(h) == ARG                                # never opened
+    m = ctypes.c_int(0)
+    assert L.ar_selftest_barrier(0, 0, 10, 1000, ctypes.byref(m)) == ARG
+    assert L.ar_selftest_barrier(0, 17, 10, 1000, ctypes.byref(m)) == ARG
+    assert L.ar_selftest_barrier(0, 2, 0, 1000, ctypes.byref(m)) == ARG
+    assert L.ar_selftest_barrier(0, 2, 10, 0, ctypes.byref(m)) == ARG
+
+
 def test_mapped_entry_point_checks_arguments_before_touching_memory(arlib):
     """ar_rmsnorm_mapped runs the same shape, alignment and alias checks as
     ar_rmsnorm before its per-pointer memory-type checks; on a machine
@@ -158,6 +254,10 @@ def _check_plan(p, n, m, H, mode):
     assert p["mode"] in (1, 2) and (mode == 0 or p["mode"] == mode)
     assert p["launches"] == (2 if p["mode"] == 2 else 1)
     assert p["vpt"] in (1, 2, 4, 8)
+    # L2 prefetch: every kernel prefetches its first row before the wait on the
+    # previous grid; a register kernel with one CTA per row may also prefetch
+    # the row one wave ahead
+    assert p["prefetch"] in ((2,) if p["kernel"] == 2 else (2, 3) if p["cluster"] == 1 else (2,))
     if p["kernel"] in (1, 3):   # register kernel: one CTA or a cluster per row
         per_cta = -(-P // p["cluster"])
         assert p["cluster"] in (1, 2, 4, 8, 16) and p["stages"] == 0

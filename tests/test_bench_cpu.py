@@ -75,3 +75,22 @@ def test_every_kernel_candidate_names_a_forced_shape():
         assert kernel in ("stream", "register", "register_late")
         assert (vpt == 0) == (kernel == "stream")
         assert name.endswith(str(vpt)) or kernel == "stream"
+
+
+def test_cpu_baseline_times_one_thread_and_all_threads():
+    """The CPU baseline reports the oracle single-threaded and over every host
+    thread, each the fastest of 3 passes, with the CPU model."""
+    import oracle
+    import synth
+    from oracle import build as oracle_build
+    oracle_build.build()
+    w = synth.TINY
+    inp = synth.make_inputs(w, 64)
+    cb = bench.cpu_baseline(inp, w.n, w.H, w.eps, False, budget_s=0.3)
+    assert cb["kind"] == "oracle" and cb["unit"] == "GB/s" and cb["value"] > 0
+    assert cb["cores"] == oracle.host_threads() and cb["cpu_model"]
+    st = cb["single_thread"]
+    assert st["cores"] == 1 and st["value"] > 0 and "1 thread" in st["sample"]
+    assert "fastest of 3" in cb["sample"] and "fastest of 3" in st["sample"]
+    assert cb["speedup_all_threads"] == round(cb["value"] / st["value"], 2)
+    assert isinstance(bench.cpu_model(), str) and bench.cpu_model()

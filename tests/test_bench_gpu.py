@@ -32,6 +32,8 @@ def test_bench_prints_the_contract_line(arlib):
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
     cb = d["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] > 0 and cb["sample"]
+    assert cb["single_thread"]["value"] > 0 and cb["single_thread"]["cores"] == 1
+    assert cb["cpu_model"]
     e = d["e2e"]
     assert e["value"] > 0 and e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
     assert e["residual_out_equals_device_path"] is True

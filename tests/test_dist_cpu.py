@@ -124,3 +124,71 @@ def test_agree_without_a_process_group():
     sys.path.insert(0, ROOT)
     from allreduce_sum_residual_gb300 import consensus
     assert consensus.agree(True) is True and consensus.agree(False) is False
+
+
+def _peer_map_rank(rank, world, port, fail_rank, fail_at, q):
+    """One gloo rank mapping two fake buffers: handles are (rank, index)
+    pairs, 'opening' one yields a made-up address; a failure is injected on
+    `fail_rank` while getting its handles or while opening a peer's."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from allreduce_sum_residual_gb300 import peers
+    dist.init_process_group("gloo")
+    opened = []
+
+    class Buf:
+        def __init__(self, i):
+            self.i = i
+
+        def data_ptr(self):
+            return 1000 * rank + self.i
+
+    def get_handle(t):
+        if rank == fail_rank and fail_at == "handle":
+            raise RuntimeError("IPC handle failure injected on this rank")
+        return bytes([rank, t.i]) + bytes(62), 16 * t.i
+
+    def open_handle(h, off):
+        if rank == fail_rank and fail_at == "open":
+            raise RuntimeError("IPC open failure injected on this rank")
+        opened.append(h)
+        return 1000 * h[0] + h[1] + off
+
+    def close_handle(h):
+        opened.remove(h)
+
+    pm = peers.map_peer_buffers([Buf(0), Buf(1)], get_handle=get_handle, open_handle=open_handle,
+                                close_handle=close_handle)
+    dist.barrier()   # every rank reached the same decision: a collective still completes
+    q.put((rank, None if pm is None else pm.addrs, len(opened)))
+    if pm is not None:
+        pm.close()
+        assert not opened
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("fail_rank,fail_at", [(None, None), (0, "handle"), (1, "handle"),
+                                               (1, "open"), (0, "open")])
+def test_peer_mapping_is_collective(fail_rank, fail_at):
+    """Every rank maps every other rank's buffers, in rank order, or -- when
+    one rank's IPC setup fails -- every rank declines and keeps nothing open."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_peer_map_rank, args=(r, 2, port, fail_rank, fail_at, q))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    if fail_rank is None:
+        # buffer i of rank r: this rank's own pointer, or the peer's handle
+        # opened at its offset (1000 r + i + 16 i)
+        assert got[0] == (0, [[0, 1000], [1, 1001 + 16]], 2)
+        assert got[1] == (1, [[0, 1000], [1 + 16, 1001]], 2)
+    else:
+        assert got == [(0, None, 0), (1, None, 0)]

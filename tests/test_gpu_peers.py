@@ -1,0 +1,193 @@
+"""The cross-rank data plane on one GPU.
+
+* The bounded flag barrier: a wait on a flag that nothing sets gives up with
+  AR_ERR_TIMEOUT and leaves the context usable; flags posted by earlier
+  kernels on the stream let it pass; epochs compare modulo 2^32.
+* All ranks of a barrier inside one cooperative kernel (they run at the same
+  time), checking that data written before a post is seen after the wait.
+* The two-shot path (stage 1 stored into every rank's temporary, barrier,
+  stage 2) with the other ranks' parts run earlier on the stream, so that
+  no kernel waits on a later one: against the oracle's two-stage result.
+* Two processes on this GPU sharing their buffers through CUDA IPC handles
+  exchanged over a gloo group: the one-shot path (every rank reads both
+  partials through the mappings) and the two-shot path (stores into both
+  ranks' temporaries, synchronised on the host, then stage 2), each rank
+  against the oracle; and the collective decline when one rank's IPC setup
+  fails.  Kernels of the two processes never wait on one another.
+"""
+import multiprocessing as mp
+import os
+import socket
+import sys
+
+import pytest
+import torch
+
+import allreduce_sum_residual_gb300 as arn
+import synth
+from gpu_helpers import compare, device_inputs, oracle_rows
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _pads(world):
+    return [torch.zeros(arn.AR_MAX_RANKS, dtype=torch.int32, device="cuda") for _ in range(world)]
+
+
+def _flags(pad, world):
+    return [int(x) & 0xFFFFFFFF for x in pad[:world].tolist()]
+
+
+def test_wait_on_a_flag_nobody_sets_times_out():
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    pads = _pads(2)
+    arn.ar_barrier(pads, 0, 1, limit_us=2000)          # rank 1 never arrives
+    assert arn.ar_device_status(0, reset=True) == arn.AR_ERR_TIMEOUT
+    assert _flags(pads[0], 2) == [1, 0] and _flags(pads[1], 2) == [1, 0]   # rank 0 did post
+    arn.ar_signal_wait(pads[1], 2, 1, limit_us=2000)   # rank 1's own flag is still unset
+    assert arn.ar_device_status(0, reset=True) == arn.AR_ERR_TIMEOUT
+    x = torch.arange(8, device="cuda", dtype=torch.float32)
+    assert float(x.sum()) == 28.0                      # the context is still usable
+    assert arn.ar_device_status(0) == arn.AR_OK
+
+
+def test_wait_passes_on_flags_posted_by_earlier_kernels():
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    pads = _pads(4)
+    for r in (1, 2, 3):
+        arn.ar_signal_post(pads, r, 7)
+    arn.ar_barrier(pads, 0, 7, limit_us=1_000_000)
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    for p in pads:
+        assert _flags(p, 4) == [7, 7, 7, 7]
+    # a flag of an older epoch does not satisfy a newer wait
+    arn.ar_signal_post(pads, 1, 8)
+    arn.ar_signal_post(pads, 2, 8)
+    arn.ar_barrier(pads, 0, 8, limit_us=2000)          # rank 3 is still at 7
+    assert arn.ar_device_status(0, reset=True) == arn.AR_ERR_TIMEOUT
+    # epochs compare modulo 2^32: 0xFFFFFFFF, then 0 and 1 after the wrap
+    pads = _pads(2)
+    for e in (0xFFFFFFFE, 0xFFFFFFFF, 0, 1):
+        arn.ar_signal_post(pads, 1, e)
+        arn.ar_barrier(pads, 0, e, limit_us=1_000_000)
+        assert arn.ar_device_status(0, reset=True) == arn.AR_OK, hex(e)
+    assert _flags(pads[0], 2) == [1, 1]
+
+
+@pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
+def test_all_ranks_of_a_barrier_in_one_cooperative_kernel(world):
+    st, stale = arn.ar_selftest_barrier(0, world, rounds=2000, limit_us=1_000_000)
+    assert st == arn.AR_OK and stale == 0
+
+
+@pytest.mark.parametrize("world,m,H", [(1, 64, 4096), (2, 77, 4104), (4, 300, 7168),
+                                       (8, 16, 6144), (3, 5, 24)])
+def test_two_shot_with_the_other_ranks_run_first(world, m, H):
+    """Ranks 1 .. world-1 run their stage 1 and post before rank 0's whole
+    two-shot call: its barrier finds every flag set (nothing waits on a
+    later launch), and its results are the two-stage results."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    w = synth.Workload("two_shot", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=world + m)
+    inp = device_inputs(w, m)
+    temps = [torch.zeros((m, H), dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    pads = _pads(world)
+    for r in range(1, world):
+        arn.ar_reduce_scatter_store(inp.partials, temps, r)
+        arn.ar_signal_post(pads, r, 1)
+    out, rout = arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps,
+                                        pads, 0, 1)
+    if arn.ar_workspace_elems(0) < m * H:
+        arn.ar_reserve_workspace(m * H, 0)
+    ref_out, ref_rout = arn.ar_rmsnorm(inp.partials, inp.residual, inp.weight, inp.eps,
+                                       mode="two_stage")
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    for t in temps[1:]:                                 # every rank's temporary holds the sum
+        assert torch.equal(t.view(torch.int16), temps[0].view(torch.int16))
+    compare((out, rout, temps[0].float()), oracle_rows(inp, None, True), f"two-shot world={world}")
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(rout.view(torch.int16), ref_rout.view(torch.int16))
+
+
+# ---------------------------------------------------------------- two processes, CUDA IPC
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _ipc_rank(rank, world, port, m, H, fail_open_rank, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK="0")
+    sys.path[:0] = [ROOT, os.path.join(ROOT, "tests")]
+    try:
+        import torch.distributed as dist
+        import allreduce_sum_residual_gb300 as arn
+        from allreduce_sum_residual_gb300 import peers
+        import synth
+        from gpu_helpers import compare, oracle_rows
+        torch.cuda.set_device(0)
+        dist.init_process_group("gloo")
+        w = synth.Workload("ipc", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=m + H)
+        inp = synth.make_inputs(w, m)              # the same seeded inputs on every rank
+        mine = inp.partials[rank].cuda()           # this rank's partial, its own allocation
+        temp = torch.zeros((m, H), dtype=torch.bfloat16, device="cuda")
+        residual, weight = inp.residual.cuda(), inp.weight.cuda()
+
+        def open_handle(h, off):
+            if rank == fail_open_rank:
+                raise RuntimeError("IPC open failure injected on this rank")
+            return arn.ar_ipc_open(h, off)
+
+        pm = peers.map_peer_buffers([mine, temp], open_handle=open_handle)
+        if pm is None:
+            dist.barrier()
+            q.put((rank, "declined"))
+            dist.destroy_process_group()
+            return
+        torch.cuda.synchronize()
+        dist.barrier()                             # every partial is written
+        full = synth.Inputs([p.cuda() for p in inp.partials], residual, weight, inp.eps)
+        # one-shot: every rank reads every rank's partial through the mappings
+        out, rout = peers.ar_rmsnorm_peers(pm[0], residual, weight, inp.eps, mode="one_stage")
+        torch.cuda.synchronize()
+        compare((out, rout, None), oracle_rows(full, None, False), f"one-shot rank {rank}")
+        # two-shot: this rank's slice into both temporaries, a host barrier, stage 2
+        peers.ar_reduce_scatter_store_peers(pm[0], pm[1], m * H, rank)
+        torch.cuda.synchronize()
+        dist.barrier()                             # every rank's stores have landed
+        out2, rout2 = arn.ar_load_rmsnorm(temp, residual, weight, inp.eps)
+        torch.cuda.synchronize()
+        compare((out2, rout2, temp.float()), oracle_rows(full, None, True), f"two-shot rank {rank}")
+        assert arn.ar_device_status(0) == arn.AR_OK
+        dist.barrier()                             # no rank still reads a peer's buffer
+        pm.close()
+        dist.destroy_process_group()
+        q.put((rank, "ok"))
+    except Exception as e:  # report instead of hanging the parent
+        q.put((rank, f"error: {type(e).__name__}: {e}"))
+        raise
+
+
+@pytest.mark.parametrize("m,H,fail_open_rank", [(64, 4096, None), (77, 4104, None),
+                                                (16, 1024, 1)])
+def test_two_processes_share_buffers_through_ipc(m, H, fail_open_rank):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_ipc_rank, args=(r, 2, port, m, H, fail_open_rank, q))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=120)
+    want = "ok" if fail_open_rank is None else "declined"
+    assert got == [(0, want), (1, want)], got
+    assert all(p.exitcode == 0 for p in procs)
