@@ -118,6 +118,8 @@ _SIGS = {
     "ar_ipc_close": (ctypes.c_int, [ctypes.c_char_p]),
     "ar_selftest_barrier": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_uint,
                                            ctypes.POINTER(ctypes.c_int)]),
+    "ar_register_occupancy": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                             ctypes.c_int]),
     "ar_checks_bounds": (ctypes.c_int, []),
     "ar_selftest_bounds": (ctypes.c_int, [ctypes.c_int]),
     "ar_strerror": (ctypes.c_char_p, [ctypes.c_int]),
@@ -403,6 +405,12 @@ def ar_get_plan_ex(n, m, H, mode, sm_count, ctas_per_sm=None):
                                 ctypes.cast(fn, _VP) if fn else None, ctypes.byref(p)),
            "ar_get_plan_ex")
     return {f: getattr(p, f) for f, _ in ar_plan_t._fields_}
+
+
+def ar_register_occupancy(inputs, vpt, late_weight, threads):
+    """CTAs per SM of the one-CTA register kernel on the current device (0 if
+    unknown)."""
+    return int(lib().ar_register_occupancy(int(inputs), int(vpt), int(late_weight), int(threads)))
 
 
 def ar_device_status(device=0, reset=False):

@@ -895,6 +895,10 @@ int ar_get_plan(int n, int64_t m, int64_t H, int mode, int sm_count, ar_plan_t *
   return make_plan(n, m, H, mode, sm_count, smem, nullptr, plan, occupancy);
 }
 
+int ar_register_occupancy(int inputs, int vpt, int late_weight, int threads) {
+  return device_register_occupancy(inputs, vpt, late_weight, threads);
+}
+
 int ar_get_plan_ex(int n, int64_t m, int64_t H, int mode, int sm_count,
                    ar_occupancy_fn ctas_per_sm, ar_plan_t *plan) {
   if (!plan || sm_count <= 0) return AR_ERR_ARG;

@@ -58,9 +58,11 @@ def peaks():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
+# The files a kernel's device code and its launch shape come from (the plan
+# table picks the instantiation and shape of the epilogue kernels).
 KERNEL_SOURCES = {
-    "k_stream_epilogue": ("common.cuh", "stream_epilogue.cuh"),
-    "k_fused_epilogue": ("common.cuh", "epilogue.cuh"),
+    "k_stream_epilogue": ("common.cuh", "stream_epilogue.cuh", "plan_table.cuh"),
+    "k_fused_epilogue": ("common.cuh", "epilogue.cuh", "plan_table.cuh"),
     "k_reduce_flat": ("common.cuh", "epilogue.cuh", "reduce_flat.cu"),
 }
 

@@ -193,6 +193,17 @@ int ar_get_plan_ex(int n, int64_t m, int64_t H, int mode, int sm_count,
                    ar_occupancy_fn ctas_per_sm, ar_plan_t *plan);
 
 /*
+ * The current device's figure for ar_occupancy_fn: CTAs per SM of the
+ * one-CTA-per-row register kernel (inputs, vpt, late_weight, threads), read
+ * once when a launching call made the device ready; 0 if unknown (no such
+ * call yet, or arguments out of range).  Makes no CUDA call beyond
+ * cudaGetDevice.  ar_get_plan_ex with this function and the device's SM
+ * count plans exactly as ar_rmsnorm does on the device.  Library utility
+ * (no passage of the pages defines it).
+ */
+int ar_register_occupancy(int inputs, int vpt, int late_weight, int threads);
+
+/*
  * As ar_rmsnorm, with two additions for testing and tuning.  The reduced sum
  * is exposed because the pages make its bit-exactness the contract: the
  * sum follows the order of the rank pointers, so it stays bit-identical

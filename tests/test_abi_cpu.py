@@ -304,14 +304,20 @@ def test_plan_spreads_small_batches(arlib):
     for m in (1, 4, 16, 32, 63):
         assert arlib.ar_get_plan(8, m, 7168, 1, sm_count=152)["cluster"] == 8
     assert arlib.ar_get_plan(4, 64, 7168, 1, sm_count=152)["cluster"] == 1
-    # prefill: rows alone fill the GPU; two persistent streaming CTAs per SM,
-    # each with a 2-slot ring of 9 x 4 KB tiles (144 KB in flight per SM)
+    # prefill: one 768-thread CTA per row, one pack per thread; with the L2
+    # prefetch one wave ahead it outran the persistent stream kernel (7.2 vs
+    # 7.07 TB/s), so the measured table picks it
     p = arlib.ar_get_plan(8, 8192, 6144, 1, sm_count=152)
+    assert p["kernel"] == 1 and p["vpt"] == 1 and p["threads"] == 768 and p["cluster"] == 1
+    assert p["ctas"] == 8192 and p["prefetch"] in (2, 3)
+    # 8 inputs, H = 8192, 1024 rows: two persistent streaming CTAs per SM,
+    # each with a 2-slot ring of 9 x 4 KB tiles (144 KB in flight per SM)
+    p = arlib.ar_get_plan(8, 1024, 8192, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 304 and p["stages"] == 2 and p["threads"] == 288
-    # 4 inputs, H = 7168, many rows: the register kernel with the weight
-    # loaded after the sums, one pack per thread (two 896-thread CTAs per SM)
-    p = arlib.ar_get_plan(4, 8192, 7168, 1, sm_count=152)
-    assert p["kernel"] == 3 and p["vpt"] == 1 and p["threads"] == 896 and p["cluster"] == 1
+    # 8 inputs, H = 8192, 512 rows: the register kernel with the weight loaded
+    # after the sums, two packs per thread
+    p = arlib.ar_get_plan(8, 512, 8192, 1, sm_count=152)
+    assert p["kernel"] == 3 and p["vpt"] == 2 and p["threads"] == 512 and p["cluster"] == 1
     # 16 inputs: one CTA per SM, 2 slots
     p = arlib.ar_get_plan(16, 8192, 6144, 1, sm_count=152)
     assert p["kernel"] == 2 and p["ctas"] == 152 and p["stages"] == 2

@@ -18,8 +18,9 @@ int main(void) {
   memset(&plan, 0, sizeof plan);
   if (ar_version() < 100) return 1;
   if (ar_select_mode(8, 8192, 6144) != AR_MODE_ONE_STAGE) return 2;
-  if (ar_get_plan(8, 8192, 6144, AR_MODE_AUTO, 152, &plan) != AR_OK) return 3;
-  if (plan.kernel != AR_KERNEL_STREAM || plan.launches != 1) return 4;
+  if (ar_get_plan(8, 1024, 8192, AR_MODE_AUTO, 152, &plan) != AR_OK) return 3;
+  if (plan.kernel != AR_KERNEL_STREAM || plan.launches != 1 || plan.prefetch != AR_PREFETCH_ROW)
+    return 4;
   if (ar_get_plan(8, 1, 7168, AR_MODE_AUTO, 152, &plan) != AR_OK || plan.cluster != 8) return 5;
   /* argument errors come back as codes before any CUDA call */
   if (ar_rmsnorm(NULL, 0, NULL, NULL, 1e-6f, 4, 1024, NULL, NULL, AR_MODE_AUTO, NULL) != AR_ERR_ARG)
