@@ -58,13 +58,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-# The files a kernel's device code and its launch shape come from (the plan
-# table picks the instantiation and shape of the epilogue kernels).
+# The files a kernel's device code comes from.
 KERNEL_SOURCES = {
-    "k_stream_epilogue": ("common.cuh", "stream_epilogue.cuh", "plan_table.cuh"),
-    "k_fused_epilogue": ("common.cuh", "epilogue.cuh", "plan_table.cuh"),
+    "k_stream_epilogue": ("common.cuh", "stream_epilogue.cuh"),
+    "k_fused_epilogue": ("common.cuh", "epilogue.cuh"),
     "k_reduce_flat": ("common.cuh", "epilogue.cuh", "reduce_flat.cu"),
 }
+# The launch-plan fields that decide a launch's instantiation and shape.
+PLAN_KEYS = ("kernel", "cluster", "vpt", "threads", "stages", "ctas", "prefetch")
 
 
 def source_hash(kernel):
@@ -77,15 +78,18 @@ def source_hash(kernel):
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel, workload):
+def ncu_traffic(kernel, workload, plan=None):
     """DRAM bytes per launch recorded by an ncu capture of this kernel, or None
-    when none exists or the kernel sources changed since it was taken."""
+    when none exists, the kernel sources changed since it was taken, or the
+    launch plan (instantiation and shape) differs from the captured one."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
         e = d[f"{kernel}@{workload}"]
         if e.get("source_hash") != source_hash(kernel):
+            return None
+        if plan is not None and any(e["plan"][k] != plan[k] for k in PLAN_KEYS):
             return None
         return float(e["dram_bytes_per_launch"])
     except Exception:
@@ -208,6 +212,19 @@ def settle(device=None):
     torch.cuda.synchronize(device)
 
 
+def launch_shield(stream, cycles=2_000_000):
+    """Keep `stream` busy for ~1 ms (a device-side sleep) before a start
+    event, so that the host has enqueued the timed work when the event
+    fires: the region then times the kernels, not the host's launch of the
+    first graph.  No-op where torch has no device sleep."""
+    import torch
+    sleep = getattr(torch.cuda, "_sleep", None)
+    if sleep is None:
+        return
+    with torch.cuda.stream(stream):
+        sleep(int(cycles))
+
+
 def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=100):
     """W warm-up steps, then exactly K steps timed with CUDA events on
     `stream`, bracketed by barrier + synchronize.  With `use_graph` the K
@@ -237,6 +254,7 @@ def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=
     torch.cuda.synchronize(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launch_shield(stream)
     t0.record(stream)
     if use_graph:
         with torch.cuda.stream(stream):
@@ -288,6 +306,7 @@ def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=No
         for _ in range(replays):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
+            launch_shield(stream)
             a.record(stream)
             g.replay()
             b.record(stream)
@@ -349,6 +368,7 @@ def unfused_torch_us(inp, stream, calls=50, replays=5):
         for _ in range(replays):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
+            launch_shield(stream)
             a.record(stream)
             g.replay()
             b.record(stream)
@@ -389,6 +409,7 @@ def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
         for _ in range(replays):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
+            launch_shield(stream)
             a.record(stream)
             g.replay()
             b.record(stream)
@@ -414,6 +435,7 @@ def empty_node_floor_us(stream, calls=2000, replays=20):
         for _ in range(replays):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
+            launch_shield(stream)
             a.record(stream)
             g.replay()
             b.record(stream)
@@ -750,7 +772,7 @@ def run_ours(args):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_kind": peak_kind, "kernel": kernel,
                 "bytes_per_launch": bytes_step,
-                "traffic": ncu_traffic(kernel, args.workload)}
+                "traffic": ncu_traffic(kernel, args.workload, plan) if m == max(w.ms) else None}
     if path == "two_stage":
         roofline["note"] = "two launches per step; achieved uses the step's algorithmic bytes"
 

@@ -40,7 +40,7 @@ def test_recorded_traffic_is_dropped_once_the_kernel_sources_change(tmp_path, mo
     csrc = tmp_path / "allreduce_sum_residual_gb300" / "csrc"
     csrc.mkdir(parents=True)
     (tmp_path / "profiles").mkdir()
-    for name in ("common.cuh", "stream_epilogue.cuh", "plan_table.cuh"):
+    for name in ("common.cuh", "stream_epilogue.cuh"):
         (csrc / name).write_text(f"// {name}\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h = bench.source_hash("k_stream_epilogue")
@@ -64,6 +64,13 @@ def test_committed_traffic_record_matches_the_current_prefill_kernel(arlib):
         rec = json.load(f)
     e = rec[f"{kernel}@prefill"]
     assert e["source_hash"] == bench.source_hash(kernel)
+    # the captured launch is the one the plan makes (the device adds the
+    # prefetch one wave ahead to the host plan's own-row prefetch)
+    for k in bench.PLAN_KEYS:
+        if k != "prefetch":
+            assert e["plan"][k] == p[k], k
+    assert bench.ncu_traffic(kernel, "prefill", e["plan"]) == e["dram_bytes_per_launch"]
+    assert bench.ncu_traffic(kernel, "prefill", dict(e["plan"], vpt=e["plan"]["vpt"] * 2)) is None
     assert 0.9 * bench.algo_bytes(8, 8192, 6144) < e["dram_bytes_per_launch"] < \
         1.1 * bench.algo_bytes(8, 8192, 6144)
 
