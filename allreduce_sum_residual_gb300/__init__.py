@@ -426,7 +426,8 @@ def ar_selftest_bounded_wait(device=0, limit_us=1000):
 
 # ---------------------------------------------------------------- cross-rank data plane
 
-AR_SIGNAL_PAD_BYTES = AR_MAX_RANKS * 4
+AR_SIGNAL_PAD_BYTES = 128
+AR_EPOCH_AUTO = 0
 AR_IPC_HANDLE_BYTES = 64
 
 
@@ -446,26 +447,27 @@ def _cur_stream(stream):
     return _VP(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
 
 
-def ar_signal_post(pads, rank, epoch, stream=None):
+def ar_signal_post(pads, rank, epoch=AR_EPOCH_AUTO, stream=None):
     """Post `epoch` of `rank` into every rank's signal pad (tensors or addresses)."""
     _check(lib().ar_signal_post(_addrs(pads), len(pads), int(rank), int(epoch) & 0xFFFFFFFF,
                                 _cur_stream(stream)), "ar_signal_post")
 
 
-def ar_signal_wait(pad, world, epoch, limit_us=1000000, stream=None):
+def ar_signal_wait(pad, world, epoch=AR_EPOCH_AUTO, limit_us=1000000, stream=None):
     """Wait (bounded) until flags 0..world-1 of `pad` reach `epoch`."""
     _check(lib().ar_signal_wait(_VP(_addr(pad)), int(world), int(epoch) & 0xFFFFFFFF,
                                 int(limit_us), _cur_stream(stream)), "ar_signal_wait")
 
 
-def ar_barrier(pads, rank, epoch, limit_us=1000000, stream=None):
+def ar_barrier(pads, rank, epoch=AR_EPOCH_AUTO, limit_us=1000000, stream=None):
     """Post, then wait on pads[rank]: a bounded barrier of len(pads) ranks."""
     _check(lib().ar_barrier(_addrs(pads), len(pads), int(rank), int(epoch) & 0xFFFFFFFF,
                             int(limit_us), _cur_stream(stream)), "ar_barrier")
 
 
-def ar_rmsnorm_two_shot(partials, residual, weight, eps, temps, pads, rank, epoch, out=None,
-                        residual_out=None, limit_us=1000000, stream=None):
+def ar_rmsnorm_two_shot(partials, residual, weight, eps, temps, pads, rank,
+                        epoch=AR_EPOCH_AUTO, out=None, residual_out=None, limit_us=1000000,
+                        stream=None):
     """Two-stage epilogue of rank `rank` of len(temps) ranks: its stage-1 slice
     stored into every rank's temporary, a barrier, stage 2 on temps[rank].
     `partials`, `temps` and `pads` are tensors or device addresses (peer or

@@ -1082,7 +1082,7 @@ static int signal_call(void *const *pads, const void *mine, int world, int rank,
 int ar_signal_post(void *const *pads, int world, int rank, uint32_t epoch, void *stream) {
   const int st = check_pads(pads, world, rank);
   if (st != AR_OK) return st;
-  return signal_call(pads, nullptr, world, rank, epoch, 0, true, false, stream);
+  return signal_call(pads, pads[rank], world, rank, epoch, 0, true, false, stream);
 }
 
 int ar_signal_wait(const void *pad, int world, uint32_t epoch, unsigned limit_us, void *stream) {

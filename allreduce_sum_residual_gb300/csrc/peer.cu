@@ -64,6 +64,9 @@ __device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t epoch, 
   }
 }
 
+// Word of a pad holding its owner's epoch counter (after the 16 flags).
+constexpr int kCounterWord = AR_MAX_RANKS;
+
 // One warp: lane d posts into rank d's pad, lane j waits for rank j's flag.
 __global__ void __launch_bounds__(32) k_signal(const __grid_constant__ SignalArgs a) {
   // Everything the previous grids wrote (stage 1's stores into the peers'
@@ -76,11 +79,26 @@ __global__ void __launch_bounds__(32) k_signal(const __grid_constant__ SignalArg
   if (!in_bounds(a.world >= 1 && a.world <= AR_MAX_RANKS && a.rank >= 0 && a.rank < a.world,
                  a.status))
     return;
+  // AR_EPOCH_AUTO: the epoch is this rank's counter, kept in its own pad and
+  // touched only by its owner's calls (in stream order): a post moves it on.
+  uint32_t epoch = a.epoch;
+  if (epoch == AR_EPOCH_AUTO) {
+    uint32_t c = 0;
+    if (t == 0) {
+      c = a.mine[kCounterWord];
+      if (a.post) {
+        c += 1u;
+        if (c == AR_EPOCH_AUTO) c = 1u;
+        a.mine[kCounterWord] = c;
+      }
+    }
+    epoch = __shfl_sync(0xFFFFFFFFu, c, 0);
+  }
   if (a.post && t < a.world) {
     fence_sys();
-    st_release_sys(a.pads[t] + a.rank, a.epoch);
+    st_release_sys(a.pads[t] + a.rank, epoch);
   }
-  if (a.wait && t < a.world && !wait_flag(a.mine + t, a.epoch, a.limit_ns))
+  if (a.wait && t < a.world && !wait_flag(a.mine + t, epoch, a.limit_ns))
     atomicExch(a.status, AR_ERR_TIMEOUT);
   __syncwarp();
 }

@@ -355,14 +355,20 @@ int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
  * each other's address spaces through IPC handles, with a collective
  * fallback when that setup fails on any rank.
  *
- * Signal pads: each rank owns a pad of AR_MAX_RANKS 32-bit flags in its own
- * device memory (16-byte aligned, zeroed before first use).  Rank r posts
+ * Signal pads: each rank owns a pad of AR_SIGNAL_PAD_BYTES in its own
+ * device memory (16-byte aligned, zeroed before first use): 32-bit flags
+ * 0 .. AR_MAX_RANKS-1, then the rank's own epoch counter.  Rank r posts
  * epoch e by storing e into flag r of every rank's pad (a system-scope fence
  * orders the writes of all previous grids on the stream before it, then a
  * release store); it waits for epoch e by spinning on its own pad until
  * every one of the first `world` flags holds e or later (acquire; a flag f
- * has reached e when (int32_t)(f - e) >= 0, so epochs may wrap).  Use a new
- * epoch for every barrier.  A wait gives up after limit_us microseconds
+ * has reached e when (int32_t)(f - e) >= 0, so epochs may wrap).  Every
+ * barrier needs a new epoch.  Either pass it (1, 2, 3, ...), or pass
+ * AR_EPOCH_AUTO: a post (or barrier) then increments the counter in this
+ * rank's own pad and uses the new value (skipping 0), and a wait alone uses
+ * the counter's current value -- so a captured CUDA graph replays with
+ * fresh epochs, as long as every rank makes the same sequence of calls.
+ * A wait gives up after limit_us microseconds
  * (1 .. 10^7), records AR_ERR_TIMEOUT in the device status word
  * (ar_device_status) and returns: a rank that never arrives is an error, not
  * a hang.  Kernels of different ranks that wait on one another must run at
@@ -370,7 +376,9 @@ int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
  * one GPU (in one or several processes): order such ranks on the host.
  * --------------------------------------------------------------------------- */
 
-#define AR_SIGNAL_PAD_BYTES (AR_MAX_RANKS * 4)
+#define AR_SIGNAL_PAD_BYTES 128   /* 32 words: 16 flags, the epoch counter,
+                                     15 reserved                            */
+#define AR_EPOCH_AUTO 0u          /* take the epoch from the pad's counter    */
 #define AR_IPC_HANDLE_BYTES 64
 
 /* Post epoch `epoch` of rank `rank` into flag `rank` of pads[0 .. world-1]

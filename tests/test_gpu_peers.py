@@ -33,7 +33,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _pads(world):
-    return [torch.zeros(arn.AR_MAX_RANKS, dtype=torch.int32, device="cuda") for _ in range(world)]
+    return [torch.zeros(arn.AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device="cuda")
+            for _ in range(world)]
 
 
 def _flags(pad, world):
@@ -69,13 +70,43 @@ def test_wait_passes_on_flags_posted_by_earlier_kernels():
     arn.ar_signal_post(pads, 2, 8)
     arn.ar_barrier(pads, 0, 8, limit_us=2000)          # rank 3 is still at 7
     assert arn.ar_device_status(0, reset=True) == arn.AR_ERR_TIMEOUT
-    # epochs compare modulo 2^32: 0xFFFFFFFF, then 0 and 1 after the wrap
+    # epochs compare modulo 2^32: 0xFFFFFFFF, then 1 and 2 after the wrap (0
+    # is AR_EPOCH_AUTO)
     pads = _pads(2)
-    for e in (0xFFFFFFFE, 0xFFFFFFFF, 0, 1):
+    for e in (0xFFFFFFFE, 0xFFFFFFFF, 1, 2):
         arn.ar_signal_post(pads, 1, e)
         arn.ar_barrier(pads, 0, e, limit_us=1_000_000)
         assert arn.ar_device_status(0, reset=True) == arn.AR_OK, hex(e)
-    assert _flags(pads[0], 2) == [1, 1]
+    assert _flags(pads[0], 2) == [2, 2]
+
+
+def test_automatic_epochs_advance_per_call_and_across_the_wrap():
+    """AR_EPOCH_AUTO: each post moves this rank's counter (in its own pad) on
+    by one, skipping 0, and a wait alone uses the counter as it stands."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    pads = _pads(3)
+    for k in range(1, 4):
+        for r in (1, 2):
+            arn.ar_signal_post(pads, r)                 # epoch = ++counter of pad r
+        arn.ar_barrier(pads, 0, limit_us=1_000_000)
+        assert arn.ar_device_status(0, reset=True) == arn.AR_OK, k
+        for p in pads:
+            assert _flags(p, 3) == [k, k, k] and int(p[arn.AR_MAX_RANKS]) == k
+    arn.ar_signal_wait(pads[1], 3, limit_us=1_000_000)  # counter 3: every flag is there
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    # across the wrap: counters at 0xFFFFFFFF move on to 1, not to 0
+    for p in pads:
+        p[arn.AR_MAX_RANKS] = -1
+    for r in (1, 2):
+        arn.ar_signal_post(pads, r)
+    arn.ar_barrier(pads, 0, limit_us=1_000_000)
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    assert all(int(p[arn.AR_MAX_RANKS]) == 1 for p in pads)
+    # one rank missing: rank 2 does not post, so rank 0 times out
+    arn.ar_signal_post(pads, 1)
+    arn.ar_barrier(pads, 0, limit_us=2000)
+    assert arn.ar_device_status(0, reset=True) == arn.AR_ERR_TIMEOUT
 
 
 @pytest.mark.parametrize("world", [1, 2, 3, 8, 16])
@@ -112,6 +143,51 @@ def test_two_shot_with_the_other_ranks_run_first(world, m, H):
     compare((out, rout, temps[0].float()), oracle_rows(inp, None, True), f"two-shot world={world}")
     assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
     assert torch.equal(rout.view(torch.int16), ref_rout.view(torch.int16))
+
+
+def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
+    """The emulated ranks' calls (the other ranks' stage 1 and posts, then
+    rank 0's two-shot call), captured once in a CUDA graph with automatic
+    epochs and replayed on new inputs: every replay synchronises on a new
+    epoch and matches the oracle."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    world, m, H = 4, 48, 2056
+    w = synth.Workload("two_shot_graph", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m)
+    temps = [torch.zeros((m, H), dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    pads = _pads(world)
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    stream = torch.cuda.Stream()
+
+    def call():
+        for r in range(1, world):
+            arn.ar_reduce_scatter_store(inp.partials, temps, r, stream=stream)
+            arn.ar_signal_post(pads, r, stream=stream)
+        arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps, pads, 0,
+                                out=out, residual_out=rout, stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        call()                                         # eager: epoch 1
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    for replay in range(3):                            # epochs 2, 3, 4
+        fresh = device_inputs(synth.Workload("two_shot_graph", n=world, H=H, ms=(m,), p_std=0.5,
+                                             res_std=1.0, seed=100 + replay), m)
+        for dst, src in zip(inp.partials + [inp.residual], fresh.partials + [fresh.residual]):
+            dst.copy_(src)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        assert arn.ar_device_status(0, reset=True) == arn.AR_OK, replay
+        compare((out, rout, temps[0].float()), oracle_rows(inp, None, True), f"replay {replay}")
+        for p in pads:
+            assert int(p[arn.AR_MAX_RANKS]) == replay + 2
 
 
 # ---------------------------------------------------------------- two processes, CUDA IPC
