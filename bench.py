@@ -420,6 +420,53 @@ def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
     return best / calls * 1e6
 
 
+def two_shot_all_ranks_us(arn, inp, stream, calls=20, replays=5):
+    """The cross-rank two-shot path with every rank on this GPU, run in turn
+    so that no kernel waits on a later launch: ranks 1 .. n-1 store their
+    stage-1 slice into all n temporaries and post their flag, then rank 0's
+    ar_rmsnorm_two_shot (its slice, the barrier -- which finds every flag
+    set -- and stage 2).  Epochs come from the signal pads, so the graph
+    replays with fresh ones.  Per-call time = fastest replay / calls."""
+    import torch
+    n = len(inp.partials)
+    temps = [torch.empty_like(inp.residual) for _ in range(n)]
+    pads = [torch.zeros(arn.AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device=inp.residual.device)
+            for _ in range(n)]
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+
+    def call():
+        for r in range(1, n):
+            arn.ar_reduce_scatter_store(inp.partials, temps, r)
+            arn.ar_signal_post(pads, r)
+        arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps, pads, 0,
+                                out=out, residual_out=rout)
+
+    settle()
+    with torch.cuda.stream(stream):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(calls):
+            call()
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            launch_shield(stream)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+    status = arn.ar_device_status(inp.residual.device.index or 0, reset=True)
+    del g, temps
+    return best / calls * 1e6, status
+
+
 def empty_node_floor_us(stream, calls=2000, replays=20):
     """Per-node time of a graph of back-to-back trivial kernels (a one-element
     fill): the launch-and-complete floor any dependent kernel chain pays."""
@@ -446,6 +493,54 @@ def empty_node_floor_us(stream, calls=2000, replays=20):
     return best / calls * 1e6
 
 
+def two_shot_rank_latency(arn, inps, eps, stream, calls, replays):
+    """Per-call time of one rank's ar_rmsnorm_two_shot (rank 0 of n = the
+    number of partials) when every peer is already there: the peers' flags
+    in every pad are set far ahead of rank 0's epochs, so its barrier never
+    waits.  Rank 0 reduces only its own slice into the n temporaries, then
+    runs stage 2 on its temporary: the single-rank critical path of the
+    cross-rank two-stage path (a timing comparator; the other slices of
+    its output are not those of this call).  Same method as graph_latency."""
+    import torch
+    n = len(inps[0].partials)
+    like = inps[0].residual
+    temps = [torch.empty_like(like) for _ in range(n)]
+    pads = [torch.zeros(arn.AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device=like.device)
+            for _ in range(n)]
+    for p in pads:
+        p[1:n] = 1 << 30                     # peers 1 .. n-1: far ahead of rank 0's epochs
+    outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
+
+    def call(i, o, r):
+        arn.ar_rmsnorm_two_shot(i.partials, i.residual, i.weight, eps, temps, pads, 0, out=o,
+                                residual_out=r)
+
+    settle()
+    with torch.cuda.stream(stream):
+        for i, (o, r) in zip(inps, outs):
+            call(i, o, r)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for c in range(calls):
+            o, r = outs[c % len(outs)]
+            call(inps[c % len(inps)], o, r)
+    best = float("inf")
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(replays):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            launch_shield(stream)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            b.synchronize()
+            best = min(best, a.elapsed_time(b) / 1e3)
+    del g
+    return best / calls
+
+
 def latency_table(arn, synth, stream, l2_bytes, quick):
     import torch
     rows = []
@@ -466,6 +561,10 @@ def latency_table(arn, synth, stream, l2_bytes, quick):
                 cold_t = graph_latency(arn, cold, mode, w.eps, stream, calls, replays)
                 entry[mode] = {"us_hot": round(hot * 1e6, 3), "us_cold": round(cold_t * 1e6, 3),
                                "gbs_cold": round(set_bytes / cold_t / 1e9, 1)}
+            hot = two_shot_rank_latency(arn, [base], w.eps, stream, calls, replays)
+            cold_t = two_shot_rank_latency(arn, cold, w.eps, stream, calls, replays)
+            entry["two_shot_one_rank"] = {"us_hot": round(hot * 1e6, 3),
+                                          "us_cold": round(cold_t * 1e6, 3)}
             rows.append(entry)
             del cold, base
             torch.cuda.empty_cache()
@@ -797,6 +896,13 @@ def run_ours(args):
                     "us": round(t_ag, 2), "gbs": round(bytes_step / t_ag / 1e3, 1),
                     "gbs_actual_bytes": round(ag_bytes / t_ag / 1e3, 1),
                     "note": "n rank slices each stored into n temporaries, then stage 2"}
+                t_ts, ts_status = two_shot_all_ranks_us(arn, inp, stream)
+                modes["two_shot_all_ranks"] = {
+                    "us": round(t_ts, 2), "gbs": round(bytes_step / t_ts / 1e3, 1),
+                    "gbs_actual_bytes": round(ag_bytes / t_ts / 1e3, 1),
+                    "status": arn.ar_strerror(ts_status),
+                    "note": "ar_rmsnorm_two_shot of rank 0 after ranks 1..n-1 ran their stage 1 "
+                            "and posted: slices into n temporaries, flag barrier, stage 2"}
             serial_t, _, _ = e2e_measure(arn, inp, step_mode, stream, 3 if args.quick else 10)
             pipe_t, h2d, d2h, link = e2e_pipelined(arn, inp, step_mode, 3 if args.quick else 10)
             e2e_t, h2d_m, d2h_m, same_rout = e2e_mapped(arn, inp, step_mode, stream,
@@ -846,6 +952,9 @@ def run_ours(args):
             "clocks": clocks,
             "latency_vs_m": lat,
             "empty_kernel_node_floor_us": round(floor, 3) if lat else None,
+            # the device status word after every timed kernel (a bounded wait
+            # that gave up would show here)
+            "device_status": arn.ar_strerror(arn.ar_device_status(local)),
         }
         print(json.dumps(result), flush=True)
     if world > 1:
