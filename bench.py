@@ -924,8 +924,9 @@ def run_ours(args):
                        "pipeline": "ar_rmsnorm on device buffers; cudaMemcpyAsync of 8 row "
                                    "blocks on 3 streams (copy in / epilogue / copy out)",
                        "serial_ms_per_step": round(serial_t * 1e3, 3)}}
-            cpu = cpu_baseline(inp, n, H, inp.eps, path == "two_stage",
-                               budget_s=2.0 if args.quick else 10.0)
+            if world == 1:   # the oracle's baseline is taken at N = 1 only
+                cpu = cpu_baseline(inp, n, H, inp.eps, path == "two_stage",
+                                   budget_s=2.0 if args.quick else 10.0)
         else:
             modes.pop(other, None)
         result = {
