@@ -347,7 +347,7 @@ static TableChoice table_choice(int inputs, int64_t m, int64_t P, int sms,
   for (int c = 0; c < kPlanCandidates; ++c) {
     int lo = m0, hi = m1;
     const TableChoice k = candidate(c);
-    if (occupancy != nullptr && k.kernel != AR_KERNEL_STREAM && m0 != m1) {
+    if (occupancy != nullptr && k.kernel != AR_KERNEL_STREAM && m0 != m1 && P <= kMaxPacksPerCta) {
       const int threads = static_cast<int>(((P + k.vpt - 1) / k.vpt + 31) / 32 * 32);
       const int per_sm = occupancy(inputs, k.vpt, k.kernel == AR_KERNEL_REGISTER_LATE_W ? 1 : 0,
                                    threads);
@@ -411,7 +411,7 @@ static void plan_register(int64_t m, int64_t P, int inputs, int force_cluster, i
   if (force_cluster > 0) S = force_cluster;
   const int64_t per_cta = (P + S - 1) / S;
   int vpt = 1;
-  if (table_vpt > 0 && S == 1)
+  if (table_vpt > 0 && (S == 1 || P > kMaxPacksPerCta))
     vpt = table_vpt;
   else if (m >= 1024)
     vpt = (inputs >= 4 || (inputs == 1 && per_cta > 512)) ? 2 : 1;
@@ -492,13 +492,16 @@ static bool plan_stream(int64_t m, int64_t P, int inputs, int sms, int smem_opti
   return true;
 }
 
-// CTAs of a one-CTA-per-row register-kernel plan that run at once on the
-// device (its occupancy x SMs); 0 if unknown or not that kind of plan.
-static int64_t resident_ctas(const ar_plan_t &pl, int inputs, int sms, OccupancyFn occupancy) {
-  if (occupancy == nullptr || pl.cluster != 1 || pl.kernel == AR_KERNEL_STREAM) return 0;
+// Rows a register-kernel plan works on at once on the device: its CTAs per
+// SM x SMs / CTAs per row; 0 if unknown or a stream-kernel plan.  For a
+// row split over a cluster the one-CTA instantiation's occupancy at the
+// same thread count stands in for the cluster copy's (only a prefetch
+// distance depends on it).
+static int64_t resident_rows(const ar_plan_t &pl, int inputs, int sms, OccupancyFn occupancy) {
+  if (occupancy == nullptr || pl.kernel == AR_KERNEL_STREAM || pl.cluster < 1) return 0;
   const int per_sm =
       occupancy(inputs, pl.vpt, pl.kernel == AR_KERNEL_REGISTER_LATE_W ? 1 : 0, pl.threads);
-  return per_sm > 0 ? static_cast<int64_t>(per_sm) * sms : 0;
+  return per_sm > 0 ? static_cast<int64_t>(per_sm) * sms / pl.cluster : 0;
 }
 
 // L2 prefetch of the epilogue kernel, measured on GB300 (cold buffers,
@@ -513,7 +516,7 @@ static int64_t resident_ctas(const ar_plan_t &pl, int inputs, int sms, Occupancy
 static int plan_prefetch(const ar_plan_t &pl, int64_t m, int inputs, int sms,
                          OccupancyFn occupancy) {
   if (pl.kernel == AR_KERNEL_STREAM) return AR_PREFETCH_ROW;
-  const int64_t wave = resident_ctas(pl, inputs, sms, occupancy);
+  const int64_t wave = resident_rows(pl, inputs, sms, occupancy);
   return wave > 0 && m > wave ? AR_PREFETCH_ROW_AHEAD : AR_PREFETCH_ROW;
 }
 
@@ -541,7 +544,6 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
       return AR_ERR_ARG;
     if (force->prefetch < AR_PREFETCH_AUTO || force->prefetch > AR_PREFETCH_ROW_AHEAD)
       return AR_ERR_ARG;
-    if (force->prefetch == AR_PREFETCH_ROW_AHEAD && fc > 1) return AR_ERR_ARG;
   }
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
@@ -569,7 +571,6 @@ static int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_op
   pl->launches = pl->mode == AR_MODE_TWO_STAGE ? 2 : 1;
   pl->prefetch = plan_prefetch(*pl, m, inputs, sms, occupancy);
   if (force && force->prefetch != AR_PREFETCH_AUTO) {
-    if (force->prefetch == AR_PREFETCH_ROW_AHEAD && pl->cluster > 1) return AR_ERR_ARG;
     pl->prefetch = force->prefetch;
   }
   return AR_OK;
@@ -673,7 +674,7 @@ static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n
   a->status = status;
   a->prefetch_own = pl.prefetch == AR_PREFETCH_ROW || pl.prefetch == AR_PREFETCH_ROW_AHEAD;
   a->ahead = 0;
-  if (pl.prefetch == AR_PREFETCH_ROW_AHEAD && pl.cluster == 1) {
+  if (pl.prefetch == AR_PREFETCH_ROW_AHEAD) {
     int sms = 0;
     const DeviceState *d = nullptr;
     int dev = -1;
@@ -683,7 +684,7 @@ static void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n
     } else {
       cudaGetLastError();
     }
-    if (d != nullptr) a->ahead = resident_ctas(pl, n, sms, device_register_occupancy);
+    if (d != nullptr) a->ahead = resident_rows(pl, n, sms, device_register_occupancy);
   }
 }
 

@@ -328,13 +328,18 @@ def test_plan_spreads_small_batches(arlib):
     # H above the stream kernel's limit: the register kernel with a cluster
     p = arlib.ar_get_plan(3, 1000, 65536, 1, sm_count=152)
     assert p["kernel"] == 1 and p["cluster"] == 8
-    # rows of more than 1024 packs: stream for >= 5 inputs from 256 rows,
-    # for 4 inputs from max(4 x SMs, 1024) rows
-    assert arlib.ar_get_plan(8, 255, 16384, 1, sm_count=152)["kernel"] == 1
-    assert arlib.ar_get_plan(8, 256, 16384, 1, sm_count=152)["kernel"] == 2
-    assert arlib.ar_get_plan(4, 1023, 16384, 1, sm_count=152)["kernel"] == 1
-    assert arlib.ar_get_plan(4, 1024, 16384, 1, sm_count=152)["kernel"] == 2
-    assert arlib.ar_get_plan(4, 1215, 16384, 1, sm_count=304)["kernel"] == 1
+    # rows of 1536 and 2048 packs (H = 12288, 16384) are in the measured table:
+    # the register kernel over a 2-CTA cluster per row, or the stream kernel
+    p = arlib.ar_get_plan(8, 256, 16384, 1, sm_count=152)
+    assert p["kernel"] == 1 and p["cluster"] == 2 and p["vpt"] == 2
+    assert arlib.ar_get_plan(8, 16384, 16384, 1, sm_count=152)["kernel"] == 2
+    # rows beyond the table (more than 2048 packs): stream for >= 5 inputs
+    # from 256 rows, for 4 inputs from max(4 x SMs, 1024) rows
+    assert arlib.ar_get_plan(8, 255, 24576, 1, sm_count=152)["kernel"] == 1
+    assert arlib.ar_get_plan(8, 256, 24576, 1, sm_count=152)["kernel"] == 2
+    assert arlib.ar_get_plan(4, 1023, 24576, 1, sm_count=152)["kernel"] == 1
+    assert arlib.ar_get_plan(4, 1024, 24576, 1, sm_count=152)["kernel"] == 2
+    assert arlib.ar_get_plan(4, 1215, 24576, 1, sm_count=304)["kernel"] == 1
 
 
 def plan_table():
@@ -386,12 +391,16 @@ def _cand_char(c):
     return "S1248abcd"[c]
 
 
-def _expect(p, ch):
+def _expect(p, ch, P=None):
+    """The plan realises the table's candidate `ch`; rows of more than 1024
+    packs are split over the fewest CTAs that hold them (a cluster)."""
+    cluster = 1 if P is None or P <= 1024 else -(-P // 1024)
+    cluster = 1 << (cluster - 1).bit_length() if cluster > 1 else 1
     if ch == "S":
         return p["kernel"] == 2
     if ch in "abcd":
         return p["kernel"] == 3 and p["cluster"] == 1 and p["vpt"] == 1 << "abcd".index(ch)
-    return p["kernel"] == 1 and p["cluster"] == 1 and p["vpt"] == int(ch)
+    return p["kernel"] == 1 and p["cluster"] == cluster and p["vpt"] == int(ch)
 
 
 def test_plan_follows_the_measured_table_at_every_grid_point(arlib):
@@ -402,7 +411,7 @@ def test_plan_follows_the_measured_table_at_every_grid_point(arlib):
                 s = score[i][j][k]
                 ch = _cand_char(max(range(len(s)), key=lambda c: (s[c], -c)))
                 p = arlib.ar_get_plan(n, m, 8 * P, 1, sm_count=sms)
-                assert _expect(p, ch), (n, P, m, ch, p)
+                assert _expect(p, ch, P), (n, P, m, ch, p)
 
 
 def test_plan_between_grid_points(arlib):
@@ -424,7 +433,7 @@ def test_plan_between_grid_points(arlib):
             assert p["kernel"] == 1 and p["cluster"] >= 1
             continue
         ch = _table_pick(grid, sms, score, inputs, m, H // 8, sm)
-        assert _expect(p, ch), (n, m, H, mode, sm, ch, p)
+        assert _expect(p, ch, H // 8), (n, m, H, mode, sm, ch, p)
 
 
 def _table_pick_waves(grid, sms_table, score, n, m, P, sms, occ):
@@ -441,7 +450,7 @@ def _table_pick_waves(grid, sms_table, score, n, m, P, sms, occ):
     best, best_mean = 0, -1.0
     for c in range(nc):
         lo, hi = m0, m1
-        if c > 0 and m0 != m1:
+        if c > 0 and m0 != m1 and P <= 1024:
             vpt = 1 << ((c - 1) % 4)
             late = 1 if c >= 5 else 0
             threads = -(-(-(-P // vpt)) // 32) * 32
@@ -484,7 +493,7 @@ def test_wave_aware_plan_with_given_occupancy(arlib):
         sm = rng.choice((sms, 132, 160))
         p = arlib.ar_get_plan_ex(n, m, H, 1, sm, occ)
         ch = _table_pick_waves(grid, sms, score, n, m, H // 8, sm, occ)
-        assert _expect(p, ch), (n, m, H, sm, ch, p)
+        assert _expect(p, ch, H // 8), (n, m, H, sm, ch, p)
         plain = arlib.ar_get_plan_ex(n, m, H, 1, sm, None)
         assert plain == arlib.ar_get_plan(n, m, H, 1, sm_count=sm)
         differ += plain != p
