@@ -418,8 +418,11 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
  * CUDA IPC handle (AR_IPC_HANDLE_BYTES bytes into `handle`) of the
  * allocation holding the device pointer `ptr`, and ptr's byte offset in it
  * (an IPC handle names a whole allocation).  Send both to the other ranks.
- * AR_ERR_ARG when ptr is not device memory of this process.  The setup of
- * tokenspeed #968's IPC path (Summary), in this library's C ABI.
+ * AR_ERR_ARG when ptr is not device memory of this process; AR_ERR_CUDA
+ * when the runtime has no IPC handle for it (memory from the virtual memory
+ * management API, cuMemCreate -- e.g. a caching allocator with expandable
+ * segments -- has none; the peer mapping then declines on every rank).  The
+ * setup of tokenspeed #968's IPC path (Summary), in this library's C ABI.
  */
 int ar_ipc_get_handle(const void *ptr, void *handle, int64_t *offset);
 
