@@ -34,12 +34,12 @@ def device_inputs(w, m, seed=None, big=None):
                         inp.eps)
 
 
-def run_gpu(inp, mode, cluster=0, vpt=0, with_sum=True, stream=None, kernel=0):
+def run_gpu(inp, mode, cluster=0, vpt=0, with_sum=True, stream=None, kernel=0, prefetch=0):
     m, H = inp.residual.shape
     s = torch.empty((m, H), dtype=torch.float32, device=inp.residual.device) if with_sum else None
     out, rout, s = arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, inp.eps, mode=mode,
                                      sum_out=s, cluster=cluster, vpt=vpt, stream=stream,
-                                     kernel=kernel)
+                                     kernel=kernel, prefetch=prefetch)
     return out, rout, s
 
 

@@ -196,6 +196,52 @@ def test_many_rows_of_a_very_wide_hidden_size(mode):
     check_sampled(inp, mode, f"wide/{mode}", k=24)
 
 
+@pytest.mark.parametrize("n,m,H", [(4, 1024, 16384), (8, 300, 12288), (2, 700, 16384),
+                                   (16, 200, 12288), (3, 96, 12296)])
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_wide_rows_planned_from_the_table(n, m, H, mode):
+    """Rows of 1025-2048 packs are planned from the table's widest columns:
+    the register kernel over a 2-CTA cluster per row (prefetching one wave
+    ahead when the rows need more than one wave), or the stream kernel."""
+    w = synth.Workload("wide_table", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=m + n)
+    inp = device_inputs(w, m)
+    p = arn.ar_get_plan(n, m, H, mode)
+    assert p["kernel"] == arn.AR_KERNEL_STREAM or p["cluster"] == 2, p
+    check_sampled(inp, mode, f"wide table n={n} m={m} H={H}/{mode}", k=32)
+    assert arn.ar_device_status(0) == arn.AR_OK
+
+
+PREFETCH_CASES = [
+    # (n, m, H, kernel, cluster, vpt): one CTA per row, late weight, cluster, wide rows, stream
+    (8, 400, 4096, "register", 1, 1), (4, 700, 7168, "register_late", 1, 1),
+    (8, 9, 7168, "register", 8, 1), (4, 500, 16384, "register", 2, 2),
+    (8, 300, 6144, "stream", 0, 0), (1, 1000, 2056, "register", 1, 2)]
+
+
+@pytest.mark.parametrize("n,m,H,kernel,cluster,vpt", PREFETCH_CASES)
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+def test_prefetch_never_changes_results(n, m, H, kernel, cluster, vpt, mode):
+    """The L2 prefetch is only a hint: with it off, on the own row, or also one
+    wave (stream kernel: one row) ahead, every output bit is the same."""
+    w = synth.Workload("prefetch", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=3 * m + n)
+    inp = device_inputs(w, m)
+    runs = [run_gpu(inp, mode, cluster=cluster, vpt=vpt, kernel=kernel, prefetch=pf)
+            for pf in ("none", "row", "row_ahead")]
+    torch.cuda.synchronize()
+    for other in runs[1:]:
+        for a, b in zip(runs[0], other):
+            assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else
+                               a.view(torch.int32),
+                               b.view(torch.int16) if b.dtype == torch.bfloat16 else
+                               b.view(torch.int32))
+    rows = sample_rows(m, 16)
+    idx = torch.as_tensor(rows, device="cuda")
+    out, rout, s = runs[2]
+    compare((out[idx], rout[idx], s[idx]), oracle_rows(inp, rows, mode == "two_stage"),
+            f"prefetch {kernel} n={n} m={m} H={H}/{mode}")
+    assert arn.ar_device_status(0) == arn.AR_OK
+
+
 def guarded(m, H):
     """An [m, H] bf16 view inside a buffer with 4 KiB guard bands each side,
     every guard element holding the pattern 0x5A5A."""
