@@ -944,7 +944,9 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}",
                        "timing": ("CUDA events around K steps replayed from CUDA graphs on the launch "
                        "stream" if not args.eager else "CUDA events around K eager steps")
-                      + ", max over ranks"},
+                      + ", a device sleep before the start event, max over ranks",
+                       "device": {"name": props.name, "sm_count": props.multi_processor_count,
+                                  "l2_bytes": l2, "host_cores": os.cpu_count()}},
             "pct_of_8tbs": round(value / world / 8000.0 * 100, 2),
             "roofline": roofline, "modes": modes,
             "cpu_baseline": cpu,
