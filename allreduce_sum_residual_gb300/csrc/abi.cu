@@ -29,7 +29,6 @@ EpilogueKernel epilogue_late_kernel_group0(int n, int vpt_log2);
 EpilogueKernel epilogue_late_kernel_group1(int n, int vpt_log2);
 EpilogueKernel epilogue_late_kernel_group2(int n, int vpt_log2);
 EpilogueKernel epilogue_late_kernel_group3(int n, int vpt_log2);
-EpilogueKernel epilogue_flag_kernel(int vpt_log2, bool clustered, bool late_weight);
 cudaError_t launch_reduce_flat(const ReduceArgs &a, int n, int sms, cudaStream_t stream);
 StreamKernel stream_kernel_group0(int n, int vpt_log2);
 StreamKernel stream_kernel_group1(int n, int vpt_log2);
@@ -43,11 +42,10 @@ constexpr int kAssumedSmemOptin = 232448;         // sm_100-class opt-in per CTA
 
 static int vpt_log2(int vpt) { return vpt == 1 ? 0 : vpt == 2 ? 1 : vpt == 4 ? 2 : vpt == 8 ? 3 : -1; }
 
-EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered, bool late_weight, bool flag_wait) {
+EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered, bool late_weight) {
   const int l = vpt_log2(vpt);
   if (n < 1 || n > AR_MAX_RANKS || l < 0) return nullptr;
   if (clustered && late_weight) return nullptr;
-  if (flag_wait) return n == 1 ? epilogue_flag_kernel(l, clustered, late_weight) : nullptr;
   if (late_weight) switch ((n - 1) / 4) {
       case 0: return epilogue_late_kernel_group0(n, l);
       case 1: return epilogue_late_kernel_group1(n, l);
@@ -154,16 +152,14 @@ static DeviceState *current_device(int *status) {
       }
     // Rows split over up to 16 CTAs need the non-portable cluster size.
     for (int n = 1; n <= AR_MAX_RANKS; ++n)
-      for (int vpt = 1; vpt <= 8; vpt *= 2)
-        for (int flag = 0; flag <= (n == 1 ? 1 : 0); ++flag) {
-          if (cudaFuncSetAttribute(
-                  reinterpret_cast<const void *>(epilogue_kernel(n, vpt, true, false, flag != 0)),
-                  cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-            cudaGetLastError();
-            *status = AR_ERR_CUDA;
-            return nullptr;
-          }
+      for (int vpt = 1; vpt <= 8; vpt *= 2) {
+        if (cudaFuncSetAttribute(reinterpret_cast<const void *>(epilogue_kernel(n, vpt, true, false)),
+                                 cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+          cudaGetLastError();
+          *status = AR_ERR_CUDA;
+          return nullptr;
         }
+      }
     fill_occupancy(dev);
     d.ready = true;
   }
@@ -612,10 +608,7 @@ static cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t
   // input (the temporary) is being written by stage 1 until then.
   if (after_prior) args.prefetch_own = 0;
   const cudaError_t e = cudaLaunchKernelEx(
-      &cfg,
-      epilogue_kernel(n, pl.vpt, pl.cluster > 1, pl.kernel == AR_KERNEL_REGISTER_LATE_W,
-                      args.flag_pad != nullptr),
-      args);
+      &cfg, epilogue_kernel(n, pl.vpt, pl.cluster > 1, pl.kernel == AR_KERNEL_REGISTER_LATE_W), args);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -1165,24 +1158,14 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
     return AR_ERR_ALIAS;
   DeviceState *d = current_device(&st);
   if (!d) return st;
-  // Stage 2 is a register kernel (its copy with the flag wait); where the
-  // plan would take the stream kernel, the register kernel is planned.
   ar_plan_t pl;
   st = make_plan(n, m, H, AR_MODE_TWO_STAGE, d->sms, d->smem_optin, nullptr, &pl,
                  device_register_occupancy);
-  if (st == AR_OK && pl.kernel == AR_KERNEL_STREAM) {
-    ar_plan_t reg;
-    std::memset(&reg, 0, sizeof reg);
-    reg.kernel = AR_KERNEL_REGISTER;
-    st = make_plan(n, m, H, AR_MODE_TWO_STAGE, d->sms, d->smem_optin, &reg, &pl,
-                   device_register_occupancy);
-  }
   if (st != AR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // Stage 1: this rank's slice, stored into every rank's temporary.  The
   // partials and temporaries of other ranks are peer mappings: no bulk
-  // prefetch there.  Its last CTA to finish posts this rank's epoch into
-  // every rank's pad (no separate barrier launch).
+  // prefetch there.
   const int64_t npacks = m * H / kPackElems;
   const int64_t per = (npacks + world - 1) / world;
   const int64_t begin = static_cast<int64_t>(rank) * per;
@@ -1197,29 +1180,24 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
     ra.begin = begin;
     ra.end = end;
     ra.status = d->status;
-    for (int e = 0; e < world; ++e) ra.pads[e] = static_cast<uint32_t *>(pads[e]);
-    ra.mine = static_cast<uint32_t *>(pads[rank]);
-    ra.post = 1;
-    ra.world = world;
-    ra.rank = rank;
-    ra.epoch = epoch;
     if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
-  } else {
-    // This rank's slice is empty (fewer packs than ranks): it only posts.
-    st = signal_call(pads, pads[rank], world, rank, epoch, 0, true, false, stream);
-    if (st != AR_OK) return st;
   }
-  // Stage 2 on this rank's (local) temporary, once every rank's flag in its
-  // pad reaches the epoch.
+  // Every rank's stores into this rank's temporary have landed.
+  st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+  if (st != AR_OK) return st;
+  // Stage 2 on this rank's (local) temporary.
   const void *temp_in[1] = {temps[rank]};
-  EpilogueArgs a;
-  fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
-                     d->status);
-  a.flag_pad = static_cast<const uint32_t *>(pads[rank]);
-  a.flag_world = world;
-  a.flag_epoch = epoch;
-  a.flag_limit_ns = static_cast<uint64_t>(limit_us) * 1000u;
-  return launch_epilogue(a, 1, pl, true, s) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+  cudaError_t e;
+  if (pl.kernel == AR_KERNEL_STREAM) {
+    e = launch_stream(temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                      d->status, true, s);
+  } else {
+    EpilogueArgs a;
+    fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                       d->status);
+    e = launch_epilogue(a, 1, pl, true, s);
+  }
+  return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
 
 int ar_load_rmsnorm(const void *temp, const void *residual, const void *weight, float eps,

@@ -62,13 +62,6 @@ struct EpilogueArgs {
                                  // this one's place will read); 0: none
   uint64_t wait_limit_ns;        // bound of the cluster-exchange wait
   int *status;                   // device status word (AR_ERR_TIMEOUT on timeout)
-  // Stage 2 of the two-shot path (n = 1 only): before reading its input,
-  // wait until flags 0 .. flag_world-1 of flag_pad reach flag_epoch
-  // (AR_EPOCH_AUTO: the pad's counter), for at most flag_limit_ns.
-  const uint32_t *flag_pad;      // null: no wait
-  int flag_world;
-  uint32_t flag_epoch;
-  uint64_t flag_limit_ns;
 };
 
 // Kernel parameters of stage 1 (flat reduce of every pack across ranks).
@@ -83,15 +76,6 @@ struct ReduceArgs {
   int64_t begin;
   int64_t end;
   int *status;    // device status word (checking build: AR_ERR_BOUNDS)
-  // Two-shot stage 1: when `post`, the last CTA of the grid to finish posts
-  // `epoch` (AR_EPOCH_AUTO: the next value of mine's counter) into flag
-  // `rank` of pads[0 .. world-1], after every CTA's stores.
-  uint32_t *pads[AR_MAX_RANKS];
-  uint32_t *mine;  // this rank's pad (its counters)
-  int post;
-  int world;
-  int rank;
-  uint32_t epoch;
 };
 
 // --- bf16 <-> fp32 ----------------------------------------------------------

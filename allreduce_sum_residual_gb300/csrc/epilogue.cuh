@@ -24,7 +24,6 @@
 #pragma once
 
 #include "common.cuh"
-#include "signal.cuh"
 
 namespace arn {
 
@@ -57,14 +56,10 @@ __device__ __forceinline__ void sum_pack_in_rank_order(const uint4 *const (&p)[A
 // thread, enough for a second CTA per SM at some row lengths -- at the
 // price of one more (L2-resident) load before the output.  The launch plan
 // picks whichever is faster for the shape.
-// FW (N = 1 only): stage 2 of the two-shot path, which first waits on the
-// signal pad's flags (a separate instantiation, so that the plain stage-2
-// and n = 1 kernels keep their register counts).
-template <int N, int VPT, bool CL, bool LW = false, bool FW = false>
+template <int N, int VPT, bool CL, bool LW = false>
 __global__ void __launch_bounds__(1024 / VPT)
 k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   static_assert(!(CL && LW), "the late weight load is for one CTA per row");
-  static_assert(!FW || N == 1, "the flag wait is for stage 2 (one input)");
   __shared__ float red[33];
   __shared__ float cta_totals[kMaxClusterCtas];
   __shared__ uint64_t totals_bar;  // completes when the S cluster totals have arrived
@@ -122,22 +117,6 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
   }
   if (a.early_reads) pdl_wait_prior_grid();
   pdl_launch_dependents();
-  if constexpr (FW) {
-    // Stage 2 of the two-shot path: every rank's stage 1 has stored its
-    // slice into this rank's temporary once all flags reach the epoch (the
-    // acquire loads, then the CTA barrier, order the temporary's loads).
-    if (a.flag_pad != nullptr) {
-      if (threadIdx.x < a.flag_world &&
-          in_bounds(a.flag_world <= AR_MAX_RANKS, a.status)) {
-        const uint32_t e = a.flag_epoch != AR_EPOCH_AUTO
-                               ? a.flag_epoch
-                               : *reinterpret_cast<const volatile uint32_t *>(a.flag_pad + kCounterWord);
-        if (!wait_flag(a.flag_pad + threadIdx.x, e, a.flag_limit_ns))
-          atomicExch(a.status, AR_ERR_TIMEOUT);
-      }
-      __syncthreads();
-    }
-  }
 #pragma unroll
   for (int v = 0; v < VPT; ++v) {
     const int c = c0 + static_cast<int>(threadIdx.x) + v * T;
@@ -210,9 +189,7 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
 
 // Kernel pointer for (n, vpt, clustered, late weight); n in [1,
 // AR_MAX_RANKS], vpt in {1, 2, 4, 8}; late weight only without a cluster.
-// flag_wait: the two-shot stage-2 copy (n = 1 only).
 using EpilogueKernel = void (*)(EpilogueArgs);
-EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered, bool late_weight,
-                               bool flag_wait = false);
+EpilogueKernel epilogue_kernel(int n, int vpt, bool clustered, bool late_weight);
 
 }  // namespace arn

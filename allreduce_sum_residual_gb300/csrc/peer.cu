@@ -32,9 +32,40 @@
 
 #include "common.cuh"
 #include "peer.cuh"
-#include "signal.cuh"
 
 namespace arn {
+
+__device__ __forceinline__ void st_release_sys(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t *p) {
+  uint32_t v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_sys() { asm volatile("fence.acq_rel.sys;" ::: "memory"); }
+
+// Epoch e has been reached by a flag holding f when f - e, as a signed
+// 32-bit difference, is not negative (so epochs may wrap around).
+__device__ __forceinline__ bool reached(uint32_t f, uint32_t e) {
+  return static_cast<int32_t>(f - e) >= 0;
+}
+
+// Spin until *flag reaches epoch, for at most limit_ns; false on timeout.
+__device__ __forceinline__ bool wait_flag(const uint32_t *flag, uint32_t epoch, uint64_t limit_ns) {
+  if (reached(ld_acquire_sys(flag), epoch)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (reached(ld_acquire_sys(flag), epoch)) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// Word of a pad holding its owner's epoch counter (after the 16 flags).
+constexpr int kCounterWord = AR_MAX_RANKS;
 
 // One warp: lane d posts into rank d's pad, lane j waits for rank j's flag.
 __global__ void __launch_bounds__(32) k_signal(const __grid_constant__ SignalArgs a) {
@@ -56,7 +87,8 @@ __global__ void __launch_bounds__(32) k_signal(const __grid_constant__ SignalArg
     if (t == 0) {
       c = a.mine[kCounterWord];
       if (a.post) {
-        c = next_epoch(c);
+        c += 1u;
+        if (c == AR_EPOCH_AUTO) c = 1u;
         a.mine[kCounterWord] = c;
       }
     }

@@ -16,7 +16,6 @@
 // strides over the range; each step of a thread handles U packs 256 apart,
 // issuing all U*n loads before the first add.
 #include "epilogue.cuh"
-#include "signal.cuh"
 
 namespace arn {
 
@@ -58,29 +57,6 @@ k_reduce_flat(const __grid_constant__ ReduceArgs a) {
       if (idx < a.end) {
         const uint4 v = pack8(acc[u]);
         for (int d = 0; d < a.ndst; ++d) st_stream(a.dst[d] + idx, v);
-      }
-    }
-  }
-  // Two-shot: the last CTA to finish tells every rank that this rank's
-  // slice is in its temporary.  Each thread orders its own stores (into
-  // every rank's temporary, at system scope) before its CTA's arrival; the
-  // last arrival sees all of them and posts.
-  if (a.post && in_bounds(a.world >= 1 && a.world <= AR_MAX_RANKS && a.rank >= 0 &&
-                              a.rank < a.world,
-                          a.status)) {
-    fence_sys();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      const uint32_t prev = atom_add_acq_rel_gpu(a.mine + kArriveWord, 1u);
-      if (prev == gridDim.x - 1) {
-        a.mine[kArriveWord] = 0u;  // for the next call, which runs after this grid
-        uint32_t e = a.epoch;
-        if (e == AR_EPOCH_AUTO) {
-          e = next_epoch(a.mine[kCounterWord]);
-          a.mine[kCounterWord] = e;
-        }
-        fence_sys();
-        for (int d = 0; d < a.world; ++d) st_release_sys(a.pads[d] + a.rank, e);
       }
     }
   }

@@ -62,8 +62,8 @@ def peaks():
 # The files a kernel's device code comes from.
 KERNEL_SOURCES = {
     "k_stream_epilogue": ("common.cuh", "stream_epilogue.cuh"),
-    "k_fused_epilogue": ("common.cuh", "signal.cuh", "epilogue.cuh"),
-    "k_reduce_flat": ("common.cuh", "signal.cuh", "epilogue.cuh", "reduce_flat.cu"),
+    "k_fused_epilogue": ("common.cuh", "epilogue.cuh"),
+    "k_reduce_flat": ("common.cuh", "epilogue.cuh", "reduce_flat.cu"),
 }
 # The launch-plan fields that decide a launch's instantiation and shape.
 PLAN_KEYS = ("kernel", "cluster", "vpt", "threads", "stages", "ctas", "prefetch")
