@@ -502,6 +502,19 @@ def test_wave_aware_plan_with_given_occupancy(arlib):
         arlib.ar_get_plan_ex(4, 100, 4096, 1, 0, occ)
 
 
+def test_device_occupancy_is_unknown_without_a_ready_device(arlib):
+    """ar_register_occupancy reads the table a launching call fills; before
+    that (here: no GPU at all) it is 0, and planning with it is the plain
+    interpolation."""
+    L = arlib.lib()
+    assert L.ar_register_occupancy(4, 1, 0, 512) == 0
+    assert L.ar_register_occupancy(0, 1, 0, 512) == 0 and L.ar_register_occupancy(4, 3, 0, 512) == 0
+    for n, m, H in ((4, 300, 7168), (8, 8192, 6144), (2, 1000, 2880)):
+        assert arlib.ar_get_plan_ex(n, m, H, 1, 152, L.ar_register_occupancy) == \
+            arlib.ar_get_plan(n, m, H, 1, sm_count=152)
+    assert L.ar_checks_bounds() == 0
+
+
 def test_plan_rejects_bad_shapes(arlib):
     with pytest.raises(arlib.ArError):
         arlib.ar_get_plan(8, 4, 1020, 1, sm_count=152)
