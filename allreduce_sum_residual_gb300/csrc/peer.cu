@@ -31,6 +31,7 @@
 #include <string>
 
 #include "common.cuh"
+#include "host.cuh"
 #include "peer.cuh"
 
 namespace arn {
@@ -280,6 +281,158 @@ int ar_ipc_close(const void *handle) {
     return AR_ERR_CUDA;
   }
   return AR_OK;
+}
+
+// ---------------------------------------------------------------- signals, barrier, two-shot
+
+static int check_pads(void *const *pads, int world, int rank) {
+  if (world < 1 || world > AR_MAX_RANKS || rank < 0 || rank >= world || !pads) return AR_ERR_ARG;
+  for (int d = 0; d < world; ++d)
+    if (!pads[d]) return AR_ERR_ARG;
+  for (int d = 0; d < world; ++d)
+    if (!aligned16(pads[d])) return AR_ERR_ALIGN;
+  return AR_OK;
+}
+
+static int signal_call(void *const *pads, const void *mine, int world, int rank, uint32_t epoch,
+                       unsigned limit_us, bool post, bool wait, void *stream) {
+  if (wait && (limit_us == 0 || limit_us > 10000000u)) return AR_ERR_ARG;
+  int st;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  SignalArgs a;
+  std::memset(&a, 0, sizeof a);
+  if (post)
+    for (int k = 0; k < world; ++k) a.pads[k] = static_cast<uint32_t *>(pads[k]);
+  a.mine = static_cast<uint32_t *>(const_cast<void *>(mine));
+  a.world = world;
+  a.rank = rank;
+  a.post = post;
+  a.wait = wait;
+  a.epoch = epoch;
+  a.limit_ns = static_cast<uint64_t>(limit_us) * 1000u;
+  a.status = d->status;
+  return launch_signal(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? AR_OK : AR_ERR_CUDA;
+}
+
+int ar_signal_post(void *const *pads, int world, int rank, uint32_t epoch, void *stream) {
+  const int st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  return signal_call(pads, pads[rank], world, rank, epoch, 0, true, false, stream);
+}
+
+int ar_signal_wait(const void *pad, int world, uint32_t epoch, unsigned limit_us, void *stream) {
+  if (!pad || world < 1 || world > AR_MAX_RANKS) return AR_ERR_ARG;
+  if (!aligned16(pad)) return AR_ERR_ALIGN;
+  return signal_call(nullptr, pad, world, 0, epoch, limit_us, false, true, stream);
+}
+
+int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned limit_us,
+               void *stream) {
+  const int st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  return signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+}
+
+int ar_selftest_barrier(int device, int world, int rounds, unsigned limit_us, int *mismatches) {
+  if (device < 0 || device >= kMaxDevices || world < 1 || world > AR_MAX_RANKS || rounds < 1 ||
+      rounds > 1000000 || limit_us == 0 || limit_us > 10000000u || !mismatches)
+    return AR_ERR_ARG;
+  int prev = -1;
+  if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  int st = AR_OK;
+  DeviceState *d = current_device(&st);
+  int *count = nullptr;
+  if (d) {
+    if (cudaMalloc(&count, sizeof(int)) != cudaSuccess || cudaMemset(count, 0, sizeof(int)) != cudaSuccess ||
+        launch_barrier_selftest(world, rounds, static_cast<uint64_t>(limit_us) * 1000u, d->status,
+                                count) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess ||
+        cudaMemcpy(mismatches, count, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) {
+      cudaGetLastError();
+      st = AR_ERR_CUDA;
+    }
+    if (count) cudaFree(count);
+  }
+  cudaSetDevice(prev);
+  if (st != AR_OK) return st;
+  return ar_device_status(device, 1);
+}
+
+int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, int rank, int world, void *const *temps,
+                        void *const *pads, uint32_t epoch, unsigned limit_us, void *stream) {
+  int st = check_shape(n, m, H, eps);
+  if (st != AR_OK) return st;
+  st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  if (limit_us == 0 || limit_us > 10000000u) return AR_ERR_ARG;
+  if (m == 0) return AR_OK;
+  if (!temps) return AR_ERR_ARG;
+  for (int e = 0; e < world; ++e)
+    if (!temps[e]) return AR_ERR_ARG;
+  for (int e = 0; e < world; ++e)
+    if (!aligned16(temps[e])) return AR_ERR_ALIGN;
+  st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, nullptr);
+  if (st != AR_OK) return st;
+  const int64_t bytes = m * H * 2;
+  for (int e = 0; e < world; ++e) {
+    const Range t = range_of(temps[e], bytes);
+    for (int k = 0; k < n; ++k)
+      if (overlap(t, range_of(partials[k], bytes))) return AR_ERR_ALIAS;
+    for (int f = e + 1; f < world; ++f)
+      if (overlap(t, range_of(temps[f], bytes))) return AR_ERR_ALIAS;
+  }
+  const Range mine = range_of(temps[rank], bytes);
+  if (overlap(mine, range_of(out, bytes)) || overlap(mine, range_of(residual_out, bytes)) ||
+      overlap(mine, range_of(residual, bytes)) || overlap(mine, range_of(weight, H * 2)))
+    return AR_ERR_ALIAS;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  ar_plan_t pl;
+  st = make_plan(n, m, H, AR_MODE_TWO_STAGE, d->sms, d->smem_optin, nullptr, &pl,
+                 device_register_occupancy);
+  if (st != AR_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Stage 1: this rank's slice, stored into every rank's temporary.  The
+  // partials and temporaries of other ranks are peer mappings: no bulk
+  // prefetch there.
+  const int64_t npacks = m * H / kPackElems;
+  const int64_t per = (npacks + world - 1) / world;
+  const int64_t begin = static_cast<int64_t>(rank) * per;
+  const int64_t end = begin + per < npacks ? begin + per : npacks;
+  if (begin < end) {
+    ReduceArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    for (int k = 0; k < n; ++k) ra.p[k] = static_cast<const uint4 *>(partials[k]);
+    for (int e = 0; e < world; ++e) ra.dst[e] = static_cast<uint4 *>(temps[e]);
+    ra.ndst = world;
+    ra.prefetch = 0;
+    ra.begin = begin;
+    ra.end = end;
+    ra.status = d->status;
+    if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
+  }
+  // Every rank's stores into this rank's temporary have landed.
+  st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+  if (st != AR_OK) return st;
+  // Stage 2 on this rank's (local) temporary.
+  const void *temp_in[1] = {temps[rank]};
+  cudaError_t e;
+  if (pl.kernel == AR_KERNEL_STREAM) {
+    e = launch_stream(temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                      d->status, true, s);
+  } else {
+    EpilogueArgs a;
+    fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                       d->status);
+    e = launch_epilogue(a, 1, pl, true, s);
+  }
+  return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
 
 }  // extern "C"

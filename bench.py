@@ -272,35 +272,21 @@ def timed_steps(fn, stream, steps, warmup, world, device, use_graph=True, chunk=
     return total, total / steps
 
 
-def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=None):
-    """The pages' method: `calls` calls in one CUDA graph (cycling over the
-    input sets in `inps`), per-call time = min over replays / calls.
-    `shape` = (kernel, cluster, vpt[, threads, stages, ctas]), or a dict of
-    ar_rmsnorm_ex's plan keywords (kernel, cluster, vpt, threads, stages,
-    ctas, prefetch), forces a launch shape."""
+def graph_per_call(call, stream, calls, replays, warm=None):
+    """The pages' timing method for any step: call(c) for c = 0 .. calls-1
+    captured in one CUDA graph (after one eager pass of warm(), by default
+    call(0)), replayed once untimed, then `replays` timed replays with CUDA
+    events on `stream`, each behind a launch shield.  Returns the fastest
+    replay / calls, in seconds."""
     import torch
-    outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
-    if shape is not None and not isinstance(shape, dict):
-        shape = dict(zip(("kernel", "cluster", "vpt", "threads", "stages", "ctas"), shape))
-
-    def call(i, o, r):
-        if shape is None:
-            arn.ar_rmsnorm(i.partials, i.residual, i.weight, eps, out=o, residual_out=r, mode=mode)
-        else:
-            arn.ar_rmsnorm_ex(i.partials, i.residual, i.weight, eps, out=o, residual_out=r,
-                              mode=mode, **shape)
-
     settle()
     with torch.cuda.stream(stream):
-        for i, (o, r) in zip(inps, outs):
-            call(i, o, r)
+        (warm or (lambda: call(0)))()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         for c in range(calls):
-            i = inps[c % len(inps)]
-            o, r = outs[c % len(outs)]
-            call(i, o, r)
+            call(c)
     best = float("inf")
     with torch.cuda.stream(stream):
         g.replay()
@@ -315,6 +301,34 @@ def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=No
             best = min(best, a.elapsed_time(b) / 1e3)
     del g
     return best / calls
+
+
+def graph_latency(arn, inps, mode, eps, stream, calls=2000, replays=80, shape=None):
+    """The pages' method: `calls` calls in one CUDA graph (cycling over the
+    input sets in `inps`), per-call time = min over replays / calls.
+    `shape` = (kernel, cluster, vpt[, threads, stages, ctas]), or a dict of
+    ar_rmsnorm_ex's plan keywords (kernel, cluster, vpt, threads, stages,
+    ctas, prefetch), forces a launch shape."""
+    import torch
+    outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
+    if shape is not None and not isinstance(shape, dict):
+        shape = dict(zip(("kernel", "cluster", "vpt", "threads", "stages", "ctas"), shape))
+
+    def one(i, o, r):
+        if shape is None:
+            arn.ar_rmsnorm(i.partials, i.residual, i.weight, eps, out=o, residual_out=r, mode=mode)
+        else:
+            arn.ar_rmsnorm_ex(i.partials, i.residual, i.weight, eps, out=o, residual_out=r,
+                              mode=mode, **shape)
+
+    def call(c):
+        one(inps[c % len(inps)], *outs[c % len(outs)])
+
+    def warm():
+        for i, (o, r) in zip(inps, outs):
+            one(i, o, r)
+
+    return graph_per_call(call, stream, calls, replays, warm)
 
 
 def cold_sets(synth, w, m, base, l2_bytes, calls, cap_bytes=8 << 30):
@@ -346,37 +360,15 @@ def unfused_torch_us(inp, stream, calls=50, replays=5):
     H = inp.residual.shape[1]
     w = inp.weight.float()
 
-    def call():
+    def call(c):
         s = inp.partials[0].float()
         for p in inp.partials[1:]:
             s = s + p.float()
         r = s.to(torch.bfloat16).float() + inp.residual.float()
-        rout = r.to(torch.bfloat16)
-        out = torch.nn.functional.rms_norm(r, (H,), w, eps=inp.eps).to(torch.bfloat16)
-        return out, rout
+        r.to(torch.bfloat16)
+        torch.nn.functional.rms_norm(r, (H,), w, eps=inp.eps).to(torch.bfloat16)
 
-    settle()
-    with torch.cuda.stream(stream):
-        call()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(calls):
-            call()
-    best = float("inf")
-    with torch.cuda.stream(stream):
-        g.replay()
-        for _ in range(replays):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            launch_shield(stream)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
-    del g
-    return best / calls * 1e6
+    return graph_per_call(call, stream, calls, replays) * 1e6
 
 
 def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
@@ -391,33 +383,14 @@ def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
     out = torch.empty_like(inp.residual)
     rout = torch.empty_like(inp.residual)
 
-    def call():
+    def call(c):
         for r in range(n):
             arn.ar_reduce_scatter_store(inp.partials, temps, r)
         arn.ar_load_rmsnorm(temps[0], inp.residual, inp.weight, inp.eps, out=out, residual_out=rout)
 
-    settle()
-    with torch.cuda.stream(stream):
-        call()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(calls):
-            call()
-    best = float("inf")
-    with torch.cuda.stream(stream):
-        g.replay()
-        for _ in range(replays):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            launch_shield(stream)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
-    del g, temps
-    return best / calls * 1e6
+    t = graph_per_call(call, stream, calls, replays)
+    del temps
+    return t * 1e6
 
 
 def two_shot_all_ranks_us(arn, inp, stream, calls=20, replays=5):
@@ -426,7 +399,7 @@ def two_shot_all_ranks_us(arn, inp, stream, calls=20, replays=5):
     stage-1 slice into all n temporaries and post their flag, then rank 0's
     ar_rmsnorm_two_shot (its slice, the barrier -- which finds every flag
     set -- and stage 2).  Epochs come from the signal pads, so the graph
-    replays with fresh ones.  Per-call time = fastest replay / calls."""
+    replays with fresh ones.  Returns (per-call µs, status word after)."""
     import torch
     n = len(inp.partials)
     temps = [torch.empty_like(inp.residual) for _ in range(n)]
@@ -435,36 +408,17 @@ def two_shot_all_ranks_us(arn, inp, stream, calls=20, replays=5):
     out = torch.empty_like(inp.residual)
     rout = torch.empty_like(inp.residual)
 
-    def call():
+    def call(c):
         for r in range(1, n):
             arn.ar_reduce_scatter_store(inp.partials, temps, r)
             arn.ar_signal_post(pads, r)
         arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps, pads, 0,
                                 out=out, residual_out=rout)
 
-    settle()
-    with torch.cuda.stream(stream):
-        call()
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(calls):
-            call()
-    best = float("inf")
-    with torch.cuda.stream(stream):
-        g.replay()
-        for _ in range(replays):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            launch_shield(stream)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
+    t = graph_per_call(call, stream, calls, replays)
     status = arn.ar_device_status(inp.residual.device.index or 0, reset=True)
-    del g, temps
-    return best / calls * 1e6, status
+    del temps
+    return t * 1e6, status
 
 
 def empty_node_floor_us(stream, calls=2000, replays=20):
@@ -472,25 +426,7 @@ def empty_node_floor_us(stream, calls=2000, replays=20):
     fill): the launch-and-complete floor any dependent kernel chain pays."""
     import torch
     x = torch.zeros(1, device="cuda")
-    settle()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for _ in range(calls):
-            x.fill_(1.0)
-    best = float("inf")
-    with torch.cuda.stream(stream):
-        g.replay()
-        for _ in range(replays):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            launch_shield(stream)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
-    del g
-    return best / calls * 1e6
+    return graph_per_call(lambda c: x.fill_(1.0), stream, calls, replays) * 1e6
 
 
 def two_shot_rank_latency(arn, inps, eps, stream, calls, replays):
@@ -511,34 +447,18 @@ def two_shot_rank_latency(arn, inps, eps, stream, calls, replays):
         p[1:n] = 1 << 30                     # peers 1 .. n-1: far ahead of rank 0's epochs
     outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
 
-    def call(i, o, r):
+    def one(i, o, r):
         arn.ar_rmsnorm_two_shot(i.partials, i.residual, i.weight, eps, temps, pads, 0, out=o,
                                 residual_out=r)
 
-    settle()
-    with torch.cuda.stream(stream):
+    def call(c):
+        one(inps[c % len(inps)], *outs[c % len(outs)])
+
+    def warm():
         for i, (o, r) in zip(inps, outs):
-            call(i, o, r)
-    torch.cuda.synchronize()
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=stream):
-        for c in range(calls):
-            o, r = outs[c % len(outs)]
-            call(inps[c % len(inps)], o, r)
-    best = float("inf")
-    with torch.cuda.stream(stream):
-        g.replay()
-        for _ in range(replays):
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            launch_shield(stream)
-            a.record(stream)
-            g.replay()
-            b.record(stream)
-            b.synchronize()
-            best = min(best, a.elapsed_time(b) / 1e3)
-    del g
-    return best / calls
+            one(i, o, r)
+
+    return graph_per_call(call, stream, calls, replays, warm)
 
 
 def latency_table(arn, synth, stream, l2_bytes, quick):
