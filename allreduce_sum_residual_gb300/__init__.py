@@ -113,6 +113,10 @@ _SIGS = {
                                            ctypes.c_float, _I64, _I64, _VP, _VP, ctypes.c_int,
                                            ctypes.c_int, ctypes.POINTER(_VP), ctypes.POINTER(_VP),
                                            ctypes.c_uint32, ctypes.c_uint, _VP]),
+    "ar_rmsnorm_one_shot": (ctypes.c_int, [ctypes.POINTER(_VP), ctypes.c_int, _VP, _VP,
+                                           ctypes.c_float, _I64, _I64, _VP, _VP, ctypes.c_int,
+                                           ctypes.c_int, ctypes.POINTER(_VP), ctypes.c_uint32,
+                                           ctypes.c_uint, ctypes.c_int, _VP]),
     "ar_ipc_get_handle": (ctypes.c_int, [_VP, ctypes.c_char_p, ctypes.POINTER(_I64)]),
     "ar_ipc_open": (ctypes.c_int, [ctypes.c_char_p, _I64, ctypes.POINTER(_VP)]),
     "ar_ipc_close": (ctypes.c_int, [ctypes.c_char_p]),
@@ -489,6 +493,34 @@ def ar_rmsnorm_two_shot(partials, residual, weight, eps, temps, pads, rank,
                                    int(epoch) & 0xFFFFFFFF, int(limit_us),
                                    _stream_ptr(stream, residual.device))
     _check(st, "ar_rmsnorm_two_shot")
+    return out, residual_out
+
+
+def ar_rmsnorm_one_shot(partials, residual, weight, eps, pads, rank, epoch=AR_EPOCH_AUTO,
+                        out=None, residual_out=None, limit_us=1000000, end_barrier=True,
+                        stream=None):
+    """One-stage epilogue of rank `rank` of len(pads) ranks: a barrier, the
+    epilogue over every rank's partial (plain loads), and with `end_barrier`
+    a second barrier.  An explicit `epoch` e takes e and e + 1.  `partials`
+    and `pads` are tensors or device addresses (peer or IPC mappings for
+    other ranks); residual, weight and the outputs are tensors of this
+    device.  Returns (out, residual_out)."""
+    import torch
+    m, H = residual.shape
+    _check_tensor(residual, "residual", (m, H), None)
+    _check_tensor(weight, "weight", (H,), residual.device)
+    if out is None:
+        out = torch.empty_like(residual)
+    if residual_out is None:
+        residual_out = torch.empty_like(residual)
+    _check_tensor(out, "out", (m, H), residual.device)
+    _check_tensor(residual_out, "residual_out", (m, H), residual.device)
+    st = lib().ar_rmsnorm_one_shot(_addrs(partials), len(partials), _ptr(residual), _ptr(weight),
+                                   float(eps), m, H, _ptr(out), _ptr(residual_out), int(rank),
+                                   len(pads), _addrs(pads), int(epoch) & 0xFFFFFFFF,
+                                   int(limit_us), 1 if end_barrier else 0,
+                                   _stream_ptr(stream, residual.device))
+    _check(st, "ar_rmsnorm_one_shot")
     return out, residual_out
 
 

@@ -361,8 +361,8 @@ static bool device_accessible(const void *p, int dev) {
   }
 }
 
-static int check_mapped(const void *const *partials, int n, const void *residual,
-                        const void *weight, const void *out, const void *residual_out) {
+int check_mapped(const void *const *partials, int n, const void *residual, const void *weight,
+                 const void *out, const void *residual_out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();

@@ -46,6 +46,12 @@ int check_shape(int n, int64_t m, int64_t H, float eps);
 int check_buffers(const void *const *partials, int n, const void *residual, const void *weight,
                   int64_t m, int64_t H, const void *out, const void *residual_out,
                   const void *sum_out);
+// Every pointer usable by the current device at its own address (its own or
+// an IPC allocation, a peer GPU's memory it can reach, managed or mapped
+// pinned host memory): AR_OK, else AR_ERR_ARG (AR_ERR_CUDA if the device
+// cannot be queried).
+int check_mapped(const void *const *partials, int n, const void *residual, const void *weight,
+                 const void *out, const void *residual_out);
 
 // --- the launch plan (plan.cu)
 int select_mode(int n, int64_t m, int64_t H);

@@ -435,4 +435,48 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
   return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
 }
 
+int ar_rmsnorm_one_shot(const void *const *partials, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, int rank, int world, void *const *pads,
+                        uint32_t epoch, unsigned limit_us, int end_barrier, void *stream) {
+  int st = check_shape(n, m, H, eps);
+  if (st != AR_OK) return st;
+  st = check_pads(pads, world, rank);
+  if (st != AR_OK) return st;
+  if (limit_us == 0 || limit_us > 10000000u || (end_barrier != 0 && end_barrier != 1))
+    return AR_ERR_ARG;
+  if (m == 0) return AR_OK;
+  st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, nullptr);
+  if (st != AR_OK) return st;
+  st = check_mapped(partials, n, residual, weight, out, residual_out);
+  if (st != AR_OK) return st;
+  DeviceState *d = current_device(&st);
+  if (!d) return st;
+  // The plan of ar_rmsnorm_mapped's one-stage path: the register kernel with
+  // plain loads, no bulk prefetch (other ranks' partials are mappings).
+  ar_plan_t force, pl;
+  std::memset(&force, 0, sizeof force);
+  force.kernel = AR_KERNEL_REGISTER;
+  force.prefetch = AR_PREFETCH_NONE;
+  st = make_plan(n, m, H, AR_MODE_ONE_STAGE, d->sms, d->smem_optin, &force, &pl,
+                 device_register_occupancy);
+  if (st != AR_OK) return st;
+  // Every rank's partial is written.
+  st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+  if (st != AR_OK) return st;
+  // The epilogue over every rank's partial.  Its predecessor is the barrier
+  // kernel, which writes only flags, so the residual and weight are read
+  // before its wait and the partials after it.
+  EpilogueArgs a;
+  fill_epilogue_args(&a, partials, n, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
+                     d->status);
+  if (launch_epilogue(a, n, pl, true, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return AR_ERR_CUDA;
+  if (!end_barrier) return AR_OK;
+  // No rank reads a partial any more: each may overwrite its own.
+  const uint32_t next =
+      epoch == AR_EPOCH_AUTO ? AR_EPOCH_AUTO : (epoch + 1u == 0u ? 1u : epoch + 1u);
+  return signal_call(pads, pads[rank], world, rank, next, limit_us, true, true, stream);
+}
+
 }  // extern "C"

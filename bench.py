@@ -429,18 +429,20 @@ def empty_node_floor_us(stream, calls=2000, replays=20):
     return graph_per_call(lambda c: x.fill_(1.0), stream, calls, replays) * 1e6
 
 
-def two_shot_rank_latency(arn, inps, eps, stream, calls, replays):
-    """Per-call time of one rank's ar_rmsnorm_two_shot (rank 0 of n = the
-    number of partials) when every peer is already there: the peers' flags
-    in every pad are set far ahead of rank 0's epochs, so its barrier never
-    waits.  Rank 0 reduces only its own slice into the n temporaries, then
-    runs stage 2 on its temporary: the single-rank critical path of the
-    cross-rank two-stage path (a timing comparator; the other slices of
-    its output are not those of this call).  Same method as graph_latency."""
+def rank_latency(arn, inps, eps, stream, calls, replays, kind):
+    """Per-call time of one rank's cross-rank call (rank 0 of n = the number
+    of partials) when every peer is already there: the peers' flags in every
+    pad are set far ahead of rank 0's epochs, so its barriers never wait.
+    `kind` "two_shot": ar_rmsnorm_two_shot -- rank 0 reduces only its own
+    slice into the n temporaries, then runs stage 2 on its temporary (the
+    other slices of its output are not those of this call).  "one_shot":
+    ar_rmsnorm_one_shot -- barrier, the epilogue over all n partials,
+    barrier.  The single-rank critical path of each cross-rank path (a
+    timing comparator).  Same method as graph_latency."""
     import torch
     n = len(inps[0].partials)
     like = inps[0].residual
-    temps = [torch.empty_like(like) for _ in range(n)]
+    temps = [torch.empty_like(like) for _ in range(n)] if kind == "two_shot" else None
     pads = [torch.zeros(arn.AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device=like.device)
             for _ in range(n)]
     for p in pads:
@@ -448,8 +450,12 @@ def two_shot_rank_latency(arn, inps, eps, stream, calls, replays):
     outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in inps]
 
     def one(i, o, r):
-        arn.ar_rmsnorm_two_shot(i.partials, i.residual, i.weight, eps, temps, pads, 0, out=o,
-                                residual_out=r)
+        if kind == "two_shot":
+            arn.ar_rmsnorm_two_shot(i.partials, i.residual, i.weight, eps, temps, pads, 0, out=o,
+                                    residual_out=r)
+        else:
+            arn.ar_rmsnorm_one_shot(i.partials, i.residual, i.weight, eps, pads, 0, out=o,
+                                    residual_out=r)
 
     def call(c):
         one(inps[c % len(inps)], *outs[c % len(outs)])
@@ -481,10 +487,11 @@ def latency_table(arn, synth, stream, l2_bytes, quick):
                 cold_t = graph_latency(arn, cold, mode, w.eps, stream, calls, replays)
                 entry[mode] = {"us_hot": round(hot * 1e6, 3), "us_cold": round(cold_t * 1e6, 3),
                                "gbs_cold": round(set_bytes / cold_t / 1e9, 1)}
-            hot = two_shot_rank_latency(arn, [base], w.eps, stream, calls, replays)
-            cold_t = two_shot_rank_latency(arn, cold, w.eps, stream, calls, replays)
-            entry["two_shot_one_rank"] = {"us_hot": round(hot * 1e6, 3),
-                                          "us_cold": round(cold_t * 1e6, 3)}
+            for kind in ("two_shot", "one_shot"):
+                hot = rank_latency(arn, [base], w.eps, stream, calls, replays, kind)
+                cold_t = rank_latency(arn, cold, w.eps, stream, calls, replays, kind)
+                entry[kind + "_one_rank"] = {"us_hot": round(hot * 1e6, 3),
+                                             "us_cold": round(cold_t * 1e6, 3)}
             rows.append(entry)
             del cold, base
             torch.cuda.empty_cache()
@@ -823,6 +830,14 @@ def run_ours(args):
                     "status": arn.ar_strerror(ts_status),
                     "note": "ar_rmsnorm_two_shot of rank 0 after ranks 1..n-1 ran their stage 1 "
                             "and posted: slices into n temporaries, flag barrier, stage 2"}
+                t_os = rank_latency(arn, [inp], inp.eps, stream, 20, 5, "one_shot") * 1e6
+                modes["one_shot_one_rank"] = {
+                    "us": round(t_os, 2), "gbs": round(bytes_step / t_os / 1e3, 1),
+                    "status": arn.ar_strerror(arn.ar_device_status(
+                        inp.residual.device.index or 0, reset=True)),
+                    "note": "ar_rmsnorm_one_shot of rank 0 with every peer's flags already set: "
+                            "barrier, the epilogue over all n partials (plain loads, no L2 "
+                            "prefetch), barrier"}
             serial_t, _, _ = e2e_measure(arn, inp, step_mode, stream, 3 if args.quick else 10)
             pipe_t, h2d, d2h, link = e2e_pipelined(arn, inp, step_mode, 3 if args.quick else 10)
             e2e_t, h2d_m, d2h_m, same_rout = e2e_mapped(arn, inp, step_mode, stream,

@@ -415,6 +415,34 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
                         void *const *pads, uint32_t epoch, unsigned limit_us, void *stream);
 
 /*
+ * One-stage epilogue of rank `rank` of `world` ranks -- the one-shot
+ * all-reduce, in which every rank reads every rank's partial -- all on
+ * `stream`: ar_barrier(pads, world, rank, epoch, limit_us), after which
+ * every rank's partial is written; then the one-stage epilogue over
+ * partials[0 .. n-1] on the register kernel with plain loads, as
+ * ar_rmsnorm_mapped; then, with end_barrier = 1, a second barrier, after
+ * which no rank reads a partial any more and each may overwrite its own
+ * (ROCm/aiter #3817, Technical Details, 1stage, across processes; the two
+ * synchronisations are the cross-rank sync of the section note above).
+ *   epoch        an explicit epoch e: the second barrier uses e + 1 (1 if
+ *                that wraps to 0), so the next call passes e + 2.
+ *                AR_EPOCH_AUTO takes both from the pad's counter.
+ *   end_barrier  1, or 0 for callers whose partial buffers alternate
+ *                between calls (a buffer is written again two calls later,
+ *                after every rank has passed the next call's first
+ *                barrier, which orders the reuse).
+ * partials[k] of other ranks are peer or IPC mappings; residual, weight,
+ * out and residual_out are this device's memory.  The results are
+ * bit-identical to ar_rmsnorm_mapped's one-stage results for the same
+ * inputs.  Arguments otherwise as ar_rmsnorm_mapped and ar_barrier;
+ * AR_ERR_ARG for end_barrier other than 0 or 1.
+ */
+int ar_rmsnorm_one_shot(const void *const *partials, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, int rank, int world, void *const *pads,
+                        uint32_t epoch, unsigned limit_us, int end_barrier, void *stream);
+
+/*
  * CUDA IPC handle (AR_IPC_HANDLE_BYTES bytes into `handle`) of the
  * allocation holding the device pointer `ptr`, and ptr's byte offset in it
  * (an IPC handle names a whole allocation).  Send both to the other ranks.

@@ -174,8 +174,8 @@ def test_static_scratch_entry_point_checks_shape_first(arlib):
 
 
 def test_cross_rank_calls_check_arguments_first(arlib):
-    """The signal, barrier, two-shot and IPC calls refuse bad arguments
-    before any CUDA call."""
+    """The signal, barrier, two-shot, one-shot and IPC calls refuse bad
+    arguments before any CUDA call."""
     L = arlib.lib()
     pads = (ctypes.c_void_p * 2)(BASE, BASE + 4096)
     assert L.ar_signal_post(pads, 0, 0, 1, None) == ARG          # world
@@ -202,6 +202,16 @@ def test_cross_rank_calls_check_arguments_first(arlib):
     assert two_shot(temps=(ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (8 << 20) + 8)) == ALIGN
     assert two_shot(temps=(ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (8 << 20) + 16)) == ALIAS
     assert two_shot(temps=(ctypes.c_void_p * 2)(BASE + (8 << 20), BASE + (16 << 20))) == ALIAS
+    one_shot = lambda **k: L.ar_rmsnorm_one_shot(
+        parts, 2, BASE + (24 << 20), BASE + (28 << 20), k.get("eps", 1e-6), k.get("m", 4),
+        k.get("H", 1024), k.get("out", BASE + (32 << 20)), BASE + (36 << 20), k.get("rank", 0),
+        k.get("world", 2), k.get("pads", pads), 1, k.get("limit", 1000), k.get("end", 1), None)
+    assert one_shot(m=0) == OK and one_shot(m=0, end=0) == OK     # checks only the sizes
+    assert one_shot(eps=float("nan")) == ARG and one_shot(H=1020) == ALIGN
+    assert one_shot(rank=2) == ARG and one_shot(world=17) == ARG and one_shot(limit=0) == ARG
+    assert one_shot(end=2) == ARG and one_shot(end=-1) == ARG
+    assert one_shot(pads=(ctypes.c_void_p * 2)(BASE, BASE + 8)) == ALIGN
+    assert one_shot(out=BASE + (16 << 20)) == ALIAS               # out on a partial
     h = ctypes.create_string_buffer(64)
     off = ctypes.c_int64(0)
     assert L.ar_ipc_get_handle(None, h, ctypes.byref(off)) == ARG

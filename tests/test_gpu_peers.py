@@ -8,6 +8,9 @@
 * The two-shot path (stage 1 stored into every rank's temporary, barrier,
   stage 2) with the other ranks' parts run earlier on the stream, so that
   no kernel waits on a later one: against the oracle's two-stage result.
+* The one-shot call (barrier, epilogue over every rank's partial, barrier)
+  with the other ranks' posts run earlier: against the oracle's one-stage
+  result; a rank that never reaches the end barrier; graph replay.
 * Two processes on this GPU sharing their buffers through CUDA IPC handles
   exchanged over a gloo group: the one-shot path (every rank reads both
   partials through the mappings) and the two-shot path (stores into both
@@ -188,6 +191,110 @@ def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
         compare((out, rout, temps[0].float()), oracle_rows(inp, None, True), f"replay {replay}")
         for p in pads:
             assert int(p[arn.AR_MAX_RANKS]) == replay + 2
+
+
+def _mapped_one_stage(inp):
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    arn.ar_rmsnorm_mapped(inp.partials, inp.residual, inp.weight, inp.eps, out=out,
+                          residual_out=rout, mode="one_stage")
+    return out, rout
+
+
+@pytest.mark.parametrize("world,m,H", [(1, 64, 4096), (2, 77, 4104), (4, 300, 7168),
+                                       (8, 16, 7168), (3, 5, 24), (16, 2, 1024)])
+def test_one_shot_with_the_other_ranks_posted_first(world, m, H):
+    """Ranks 1 .. world-1 post both barriers' epochs before rank 0's one-shot
+    call (nothing waits on a later launch): its results are the oracle's
+    one-stage results and ar_rmsnorm_mapped's bits, and both barriers left
+    every flag at the second epoch."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    w = synth.Workload("one_shot", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=world + m)
+    inp = device_inputs(w, m)
+    pads = _pads(world)
+    for r in range(1, world):
+        arn.ar_signal_post(pads, r, 5)
+        arn.ar_signal_post(pads, r, 6)
+    out, rout = arn.ar_rmsnorm_one_shot(inp.partials, inp.residual, inp.weight, inp.eps, pads, 0, 5)
+    ref_out, ref_rout = _mapped_one_stage(inp)
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    for p in pads:
+        assert _flags(p, world) == [6] * world
+    compare((out, rout, None), oracle_rows(inp, None, False), f"one-shot world={world}")
+    assert torch.equal(out.view(torch.int16), ref_out.view(torch.int16))
+    assert torch.equal(rout.view(torch.int16), ref_rout.view(torch.int16))
+
+
+def test_one_shot_end_barrier_gives_up_when_a_rank_never_finishes():
+    """Rank 1 posts only the first epoch: rank 0's results are complete, its
+    second barrier records AR_ERR_TIMEOUT and the context stays usable.
+    Without the end barrier the same call passes."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    world, m, H = 2, 24, 2048
+    w = synth.Workload("one_shot_timeout", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m)
+    pads = _pads(world)
+    arn.ar_signal_post(pads, 1, 1)
+    out, rout = arn.ar_rmsnorm_one_shot(inp.partials, inp.residual, inp.weight, inp.eps, pads, 0, 1,
+                                        limit_us=2000)
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0, reset=True) == arn.AR_ERR_TIMEOUT
+    assert _flags(pads[1], world) == [2, 1]            # rank 0 did post its second epoch
+    compare((out, rout, None), oracle_rows(inp, None, False), "one-shot, end barrier timed out")
+    arn.ar_signal_post(pads, 1, 3)
+    out2, rout2 = arn.ar_rmsnorm_one_shot(inp.partials, inp.residual, inp.weight, inp.eps, pads, 0,
+                                          3, limit_us=1_000_000, end_barrier=False)
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    assert _flags(pads[1], world) == [3, 3]
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(rout2.view(torch.int16), rout.view(torch.int16))
+
+
+def test_one_shot_replays_from_a_cuda_graph_with_fresh_epochs():
+    """The other ranks' posts and rank 0's one-shot call, captured once with
+    automatic epochs and replayed on new inputs: every call advances every
+    pad's counter by two and matches the oracle."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    world, m, H = 4, 40, 3072
+    w = synth.Workload("one_shot_graph", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m)
+    pads = _pads(world)
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    stream = torch.cuda.Stream()
+
+    def call():
+        for r in range(1, world):
+            arn.ar_signal_post(pads, r, stream=stream)
+            arn.ar_signal_post(pads, r, stream=stream)
+        arn.ar_rmsnorm_one_shot(inp.partials, inp.residual, inp.weight, inp.eps, pads, 0,
+                                out=out, residual_out=rout, stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        call()                                         # eager: epochs 1 and 2
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        call()
+    for replay in range(3):
+        fresh = device_inputs(synth.Workload("one_shot_graph", n=world, H=H, ms=(m,), p_std=0.5,
+                                             res_std=1.0, seed=200 + replay), m)
+        for dst, src in zip(inp.partials + [inp.residual], fresh.partials + [fresh.residual]):
+            dst.copy_(src)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            g.replay()
+        torch.cuda.synchronize()
+        assert arn.ar_device_status(0, reset=True) == arn.AR_OK, replay
+        compare((out, rout, None), oracle_rows(inp, None, False), f"replay {replay}")
+        for p in pads:
+            assert int(p[arn.AR_MAX_RANKS]) == 2 * (replay + 2)
 
 
 # ---------------------------------------------------------------- two processes, CUDA IPC
