@@ -390,19 +390,15 @@ static int run(const void *const *partials, int n, const void *residual, const v
   if (m == 0) return AR_OK;  // nothing is read or written; pointers may be null
   st = check_buffers(partials, n, residual, weight, m, H, out, residual_out, sum_out);
   if (st != AR_OK) return st;
-  ar_plan_t register_only;
   if (mapped) {
     st = check_mapped(partials, n, residual, weight, out, residual_out);
     if (st != AR_OK) return st;
-    std::memset(&register_only, 0, sizeof register_only);
-    register_only.kernel = AR_KERNEL_REGISTER;
-    register_only.prefetch = AR_PREFETCH_NONE;  // bulk prefetches stay on device memory
-    force = &register_only;
   }
   DeviceState *d = current_device(&st);
   if (!d) return st;
   ar_plan_t pl;
-  st = make_plan(n, m, H, mode, d->sms, d->smem_optin, force, &pl, device_register_occupancy);
+  st = make_plan(n, m, H, mode, d->sms, d->smem_optin, force, &pl, device_register_occupancy,
+                 mapped);
   if (st != AR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   // The epilogue over `inputs` (the partials, or the two-stage temporary).

@@ -57,8 +57,12 @@ int check_mapped(const void *const *partials, int n, const void *residual, const
 int select_mode(int n, int64_t m, int64_t H);
 int64_t stream_smem_bytes(int inputs, int consumers, int stages);
 int64_t resident_rows(const ar_plan_t &pl, int inputs, int sms, ar_occupancy_fn occupancy);
+// `plain_loads`: the plan for buffers that may lie outside this GPU's own
+// memory (host, IPC or peer mappings): the best register-kernel candidate
+// (the stream kernel's bulk copies are left out) and no bulk L2 prefetch.
 int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
-              const ar_plan_t *force, ar_plan_t *pl, ar_occupancy_fn occupancy = nullptr);
+              const ar_plan_t *force, ar_plan_t *pl, ar_occupancy_fn occupancy = nullptr,
+              bool plain_loads = false);
 
 // --- launches (abi.cu, reduce_flat.cu)
 void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n, const void *residual,

@@ -454,12 +454,9 @@ int ar_rmsnorm_one_shot(const void *const *partials, int n, const void *residual
   if (!d) return st;
   // The plan of ar_rmsnorm_mapped's one-stage path: the register kernel with
   // plain loads, no bulk prefetch (other ranks' partials are mappings).
-  ar_plan_t force, pl;
-  std::memset(&force, 0, sizeof force);
-  force.kernel = AR_KERNEL_REGISTER;
-  force.prefetch = AR_PREFETCH_NONE;
-  st = make_plan(n, m, H, AR_MODE_ONE_STAGE, d->sms, d->smem_optin, &force, &pl,
-                 device_register_occupancy);
+  ar_plan_t pl;
+  st = make_plan(n, m, H, AR_MODE_ONE_STAGE, d->sms, d->smem_optin, nullptr, &pl,
+                 device_register_occupancy, true);
   if (st != AR_OK) return st;
   // Every rank's partial is written.
   st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);

@@ -103,17 +103,19 @@ using OccupancyFn = ar_occupancy_fn;
 // across the wave boundary does not describe the shape.  (Held out against
 // the sweep, this lifted the pick from 0.984 to 0.990 of the best candidate
 // on average.)  Candidates are compared by their mean percentage.
+// `no_stream` leaves the stream kernel (candidate 0) out.
 static TableChoice table_choice(int inputs, int64_t m, int64_t P, int sms,
-                                OccupancyFn occupancy) {
+                                OccupancyFn occupancy, bool no_stream) {
   if (m < kTableMinRows || P > last_of(kPlanPacks)) return {0, 0};
   int n0, n1, p0, p1, m0, m1;
   bracket(kPlanInputs, static_cast<double>(inputs), &n0, &n1);
   bracket(kPlanPacks, static_cast<double>(P), &p0, &p1);
   const double rows = static_cast<double>(m) * kPlanTableSms / sms;  // in the table's SMs
   bracket(kPlanRows, rows, &m0, &m1);
-  int best = 0;
+  const int first = no_stream ? 1 : 0;
+  int best = first;
   double best_mean = -1.0;
-  for (int c = 0; c < kPlanCandidates; ++c) {
+  for (int c = first; c < kPlanCandidates; ++c) {
     int lo = m0, hi = m1;
     const TableChoice k = candidate(c);
     if (occupancy != nullptr && k.kernel != AR_KERNEL_STREAM && m0 != m1 && P <= kMaxPacksPerCta) {
@@ -290,7 +292,7 @@ static int plan_prefetch(const ar_plan_t &pl, int64_t m, int inputs, int sms,
 }
 
 int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
-                     const ar_plan_t *force, ar_plan_t *pl, OccupancyFn occupancy) {
+              const ar_plan_t *force, ar_plan_t *pl, OccupancyFn occupancy, bool plain_loads) {
   if (mode != AR_MODE_AUTO && mode != AR_MODE_ONE_STAGE && mode != AR_MODE_TWO_STAGE)
     return AR_ERR_ARG;
   std::memset(pl, 0, sizeof *pl);
@@ -313,13 +315,14 @@ int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
       return AR_ERR_ARG;
     if (force->prefetch < AR_PREFETCH_AUTO || force->prefetch > AR_PREFETCH_ROW_AHEAD)
       return AR_ERR_ARG;
+    if (plain_loads && fk == AR_KERNEL_STREAM) return AR_ERR_ARG;
   }
   const int64_t P = H / kPackElems;
   const int inputs = pl->mode == AR_MODE_TWO_STAGE ? 1 : n;
   const bool shape_forced = fc != 0 || fv != 0;
-  const TableChoice choice = table_choice(inputs, m, P, sms, occupancy);
+  const TableChoice choice = table_choice(inputs, m, P, sms, occupancy, plain_loads);
   bool want_stream = fk == AR_KERNEL_STREAM;
-  if (fk == AR_KERNEL_AUTO && !shape_forced)
+  if (fk == AR_KERNEL_AUTO && !shape_forced && !plain_loads)
     want_stream = choice.kernel ? choice.kernel == AR_KERNEL_STREAM
                                 : long_rows_want_stream(inputs, m, sms);
   if (!(want_stream && plan_stream(m, P, inputs, sms, smem_optin,
@@ -342,6 +345,7 @@ int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
   if (force && force->prefetch != AR_PREFETCH_AUTO) {
     pl->prefetch = force->prefetch;
   }
+  if (plain_loads) pl->prefetch = AR_PREFETCH_NONE;
   return AR_OK;
 }
 

@@ -246,8 +246,10 @@ int ar_rmsnorm_ex(const void *const *partials, int n, const void *residual,
  * this device can reach (peer access).  The kernels read and write such buffers directly over the
  * host link (NVLink-C2C on Grace systems): no staging copy, no device memory
  * beyond the two-stage workspace.  The epilogue runs on the register kernel
- * (plain 16-byte loads and stores).  Results are bit-identical to
- * ar_rmsnorm's register kernel for the same launch shape.
+ * (plain 16-byte loads and stores), in the form and launch shape the
+ * measured table ranks best among the register-kernel candidates, without
+ * bulk L2 prefetches.  Results are bit-identical to ar_rmsnorm's register
+ * kernel for the same launch shape.
  *
  * Each pointer is checked with cudaPointerGetAttributes before anything is
  * launched: it must be device memory of the current device, managed
