@@ -1,6 +1,8 @@
 // The cross-rank data plane of the all-reduce: the buffers of every rank
-// mapped into each rank's address space (CUDA IPC handles), and a bounded
-// flag barrier between the two stages of the two-stage path.
+// mapped into each rank's address space (CUDA IPC handles), a bounded flag
+// barrier, and the two entry points built on it -- the two-shot path
+// (stage 1 into every rank's temporary, barrier, stage 2) and the one-shot
+// path (barrier, the epilogue over every rank's partial, barrier).
 //
 // ROCm/aiter #3817 "perf: optimize fused AllReduce + RMSNorm
 // (custom_all_reduce)", Technical Details, 2stage, reduce-scatter: stage 1
