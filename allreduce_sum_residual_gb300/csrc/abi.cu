@@ -71,7 +71,6 @@ StreamKernel stream_kernel(int n, int vpt) {
 
 // ---------------------------------------------------------------- per-device state
 
-
 static std::mutex g_mu;
 static DeviceState g_dev[kMaxDevices];
 
@@ -166,11 +165,9 @@ int device_register_occupancy(int inputs, int vpt, int late, int threads) {
   return g_occupancy[dev][inputs - 1][vl][late ? 1 : 0][threads / 32 - 1];
 }
 
-
 // ---------------------------------------------------------------- checks
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 
 bool overlap(const Range &a, const Range &b) { return a.lo < b.hi && b.lo < a.hi; }
 

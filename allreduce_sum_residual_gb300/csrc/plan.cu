@@ -32,19 +32,21 @@ int select_mode(int n, int64_t m, int64_t H) {
   return m <= one_stage_max_rows(n, H) ? AR_MODE_ONE_STAGE : AR_MODE_TWO_STAGE;
 }
 
-// Kernel choice from 64 rows on, for rows up to the table's longest (1024
-// packs, H = 8192): the lookup table of plan_table.cuh, measured on GB300.
+// Kernel choice from 64 rows on, for rows up to the table's longest (2048
+// packs, H = 16384): the lookup table of plan_table.cuh, measured on GB300.
 // For every (inputs, packs per row, rows) of its grid it holds each
 // candidate's speed as a percentage of the fastest there: the stream kernel
-// and the register kernel with 1, 2, 4 or 8 packs per thread (one-stage,
-// cold buffers, CUDA-graph timing; repeated sweeps agreed within 0.5 %).
+// and the register kernel with 1, 2, 4 or 8 packs per thread, with the
+// weight loaded early or late (one-stage, cold buffers, CUDA-graph timing;
+// repeated sweeps agreed within 0.5 %).  Rows of more than 1024 packs are
+// split over a 2-CTA cluster, where the late forms do not run.
 // No simple rule fits it: which kernel wins turns on how many CTAs of each
 // fit an SM (the register counts of each instantiation), whether the rows
 // fill a whole number of waves, and how many bytes are then in flight --
 // one more wave of a few rows can cost 25 %.  Between grid points the
 // percentages of the grid cells that bracket the shape (two columns per
-// axis where it falls between two: inputs, packs, rows) are added up and
-// the best sum wins, which prefers a candidate that is good on both sides
+// axis where it falls between two: inputs, packs, rows) are averaged and
+// the best mean wins, which prefers a candidate that is good on both sides
 // of a cliff.  Rows are first scaled to the table's SM count; rows
 // shorter than the table's shortest use its column.  Returns the kernel
 // and its packs per thread, or kernel 0 where the table does not apply
@@ -147,7 +149,8 @@ static TableChoice table_choice(int inputs, int64_t m, int64_t P, int sms,
   return candidate(best);
 }
 
-// Rows of more than 1024 packs (beyond the table): the stream kernel for 4
+// Rows beyond the table (more than 2048 packs), and below its shortest
+// rows column where the table does not apply: the stream kernel for 4
 // inputs from max(4 x SMs, 1024) rows and for 5 or more from 256 rows (at
 // H = 8192 the register kernel's 1024-thread CTAs fit once per SM, up to
 // 1.4x slower than the stream kernel from 256 rows at n = 8); otherwise the
@@ -167,7 +170,7 @@ static bool long_rows_want_stream(int inputs, int64_t m, int sms) {
 //    m <= 32 once the cluster exchange became one st.async per CTA pair --
 //    while from 64 rows one CTA per row was as fast or faster;
 //  * vpt: `table_vpt` where the lookup table gives one; otherwise (below 64
-//    rows, or rows of more than 1024 packs) 1 pack per thread, the most
+//    rows, or rows beyond the table) 1 pack per thread, the most
 //    loads in flight per CTA, except 2 for 256 .. 1023 rows of more than
 //    512 packs a CTA (a CTA of up to 1024 threads fits once per SM and the
 //    rows would run in two waves) and for 1024 rows or more with 4 inputs
