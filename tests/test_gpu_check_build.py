@@ -105,6 +105,42 @@ def test_stage_and_cross_rank_kernels_pass_their_checks(checklib):
         assert torch.equal(t.view(torch.int16), temps[0].view(torch.int16))
 
 
+def test_one_and_two_shot_calls_pass_their_checks(checklib):
+    """Both cross-rank entry points of the checking build, rank 0 of 4 with
+    the other ranks' posts (and stage-1 slices) run first: no check fires
+    and the results are the oracle's."""
+    torch.cuda.set_device(0)
+    world, m, H = 4, 9, 2056
+    w = synth.Workload("check_shots", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m)
+    arr = (ctypes.c_void_p * world)(*[p.data_ptr() for p in inp.partials])
+    pads = [torch.zeros(arn.AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device="cuda")
+            for _ in range(world)]
+    parr = (ctypes.c_void_p * world)(*[p.data_ptr() for p in pads])
+    temps = [torch.zeros((m, H), dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    tarr = (ctypes.c_void_p * world)(*[t.data_ptr() for t in temps])
+    out = torch.empty_like(inp.residual)
+    rout = torch.empty_like(inp.residual)
+    args = (inp.residual.data_ptr(), inp.weight.data_ptr(), inp.eps, m, H, out.data_ptr(),
+            rout.data_ptr(), 0, world)
+    for r in range(1, world):
+        assert checklib.ar_signal_post(parr, world, r, 1, None) == arn.AR_OK
+        assert checklib.ar_signal_post(parr, world, r, 2, None) == arn.AR_OK
+    assert checklib.ar_rmsnorm_one_shot(arr, world, *args, parr, 1, 1_000_000, 1,
+                                        None) == arn.AR_OK
+    torch.cuda.synchronize()
+    assert checklib.ar_device_status(0, 1) == arn.AR_OK
+    compare((out, rout, None), oracle_rows(inp, None, False), "checking build, one-shot")
+    for r in range(1, world):
+        assert checklib.ar_reduce_scatter_store(arr, world, m * H, r, world, tarr, None) == arn.AR_OK
+        assert checklib.ar_signal_post(parr, world, r, 3, None) == arn.AR_OK
+    assert checklib.ar_rmsnorm_two_shot(arr, world, *args, tarr, parr, 3, 1_000_000,
+                                        None) == arn.AR_OK
+    torch.cuda.synchronize()
+    assert checklib.ar_device_status(0, 1) == arn.AR_OK
+    compare((out, rout, None), oracle_rows(inp, None, True), "checking build, two-shot")
+
+
 def test_checks_are_live_only_in_the_checking_build(checklib):
     assert checklib.ar_selftest_bounds(0) == arn.AR_ERR_BOUNDS
     assert checklib.ar_device_status(0, 0) == arn.AR_OK       # the self-test cleared it
