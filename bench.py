@@ -1082,6 +1082,21 @@ def run_stream_shapes(args):
             torch.cuda.empty_cache()
 
 
+# AR_MODE=auto|one_stage|two_stage (or 0|1|2) forces the path of the bench's
+# timed step, as the pages' AITER_AR_1STAGE switch forces theirs (ROCm/aiter
+# #3817, Test Plan, Benchmark); the library itself takes the mode as an
+# argument.
+_ENV_MODES = {"0": "auto", "1": "one_stage", "2": "two_stage",
+              "auto": "auto", "one_stage": "one_stage", "two_stage": "two_stage"}
+
+
+def env_mode():
+    v = os.environ.get("AR_MODE", "auto").strip().lower()
+    if v not in _ENV_MODES:
+        raise SystemExit(f"AR_MODE={v!r}: expected auto, one_stage, two_stage, 0, 1 or 2")
+    return _ENV_MODES[v]
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1101,7 +1116,8 @@ def main(argv=None):
     ap.add_argument("--quick", action="store_true", help="shorter latency table and baselines")
     ap.add_argument("--no-latency", action="store_true")
     ap.add_argument("--m", type=int, default=0, help="token count (default: the workload's)")
-    ap.add_argument("--mode", default="auto", choices=("auto", "one_stage", "two_stage"))
+    ap.add_argument("--mode", default=env_mode(), choices=("auto", "one_stage", "two_stage"),
+                    help="the path (default: $AR_MODE, else auto)")
     ap.add_argument("--kernel", default="auto", choices=("auto", "register", "register_late", "stream"),
                     help="force the epilogue kernel (profiling)")
     ap.add_argument("--eager", action="store_true",

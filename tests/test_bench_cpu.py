@@ -105,3 +105,15 @@ def test_cpu_baseline_times_one_thread_and_all_threads():
     assert "fastest of 3" in cb["sample"] and "fastest of 3" in st["sample"]
     assert abs(cb["speedup_all_threads"] - cb["value"] / st["value"]) <= 0.01 * cb["speedup_all_threads"] + 0.01
     assert isinstance(bench.cpu_model(), str) and bench.cpu_model()
+
+
+def test_ar_mode_environment_picks_the_default_path(monkeypatch):
+    import bench
+    monkeypatch.delenv("AR_MODE", raising=False)
+    assert bench.env_mode() == "auto"
+    for v, want in (("1", "one_stage"), ("two_stage", "two_stage"), ("0", "auto"), (" AUTO ", "auto")):
+        monkeypatch.setenv("AR_MODE", v)
+        assert bench.env_mode() == want
+    monkeypatch.setenv("AR_MODE", "3")
+    with pytest.raises(SystemExit):
+        bench.env_mode()
