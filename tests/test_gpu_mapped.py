@@ -36,7 +36,7 @@ def _host_inputs(inp, which):
 
 @pytest.mark.parametrize("n,m,H,mode", [(2, 4, 1024, "one_stage"), (8, 16, 7168, "auto"),
                                         (3, 300, 4096, "auto"), (4, 257, 2056, "two_stage"),
-                                        (8, 1024, 6144, "auto")])
+                                        (8, 1024, 6144, "auto"), (4, 1024, 7168, "auto")])
 def test_host_buffers_match_oracle_and_device_path(n, m, H, mode):
     w = synth.Workload("mapped", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0)
     inp = device_inputs(w, m, seed=11)

@@ -296,6 +296,30 @@ def test_in_place_residual(mode):
     compare((out, rout, None), orc, f"in-place {mode}")
 
 
+@pytest.mark.parametrize("mode", ["one_stage", "two_stage"])
+@pytest.mark.parametrize("n,m,H,kernel,cluster,vpt,prefetch", [
+    (4, 300, 4104, "register", 1, 1, "row_ahead"), (4, 1024, 7168, "register_late", 1, 1, "row_ahead"),
+    (8, 700, 4096, "register", 1, 2, "row_ahead"), (8, 96, 12288, "register", 2, 1, "row"),
+    (16, 600, 4096, "stream", 0, 0, "row"), (8, 19, 7168, "register", 8, 1, "row")])
+def test_in_place_residual_every_kernel_form(mode, n, m, H, kernel, cluster, vpt, prefetch):
+    """residual_out == residual for every kernel form, with the L2 prefetch of
+    the own row and one wave ahead: a row's residual is read before its
+    residual_out overwrites it, and no row is read after another row's CTA
+    has written it."""
+    w = synth.Workload("inplace_forms", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=n + m)
+    inp = device_inputs(w, m)
+    if arn.ar_workspace_elems(0) < m * H:
+        arn.ar_reserve_workspace(m * H, 0)
+    orc = oracle_rows(inp, None, mode == "two_stage")
+    out, rout, _ = arn.ar_rmsnorm_ex(inp.partials, inp.residual, inp.weight, w.eps,
+                                     residual_out=inp.residual, mode=mode, kernel=kernel,
+                                     cluster=cluster, vpt=vpt, prefetch=prefetch)
+    torch.cuda.synchronize()
+    assert rout.data_ptr() == inp.residual.data_ptr()
+    assert arn.ar_device_status(0) == arn.AR_OK
+    compare((out, rout, None), orc, f"in-place {kernel} n={n} m={m} H={H} {mode}")
+
+
 def test_n1_two_stage_equals_one_stage():
     w = synth.Workload("n1", n=1, H=4096, ms=(64,), p_std=0.5, res_std=1.0)
     inp = device_inputs(w, 64)

@@ -202,7 +202,8 @@ def _mapped_one_stage(inp):
 
 
 @pytest.mark.parametrize("world,m,H", [(1, 64, 4096), (2, 77, 4104), (4, 300, 7168),
-                                       (8, 16, 7168), (3, 5, 24), (16, 2, 1024)])
+                                       (8, 16, 7168), (3, 5, 24), (16, 2, 1024),
+                                       (2, 100, 12288), (4, 1024, 7168)])
 def test_one_shot_with_the_other_ranks_posted_first(world, m, H):
     """Ranks 1 .. world-1 post both barriers' epochs before rank 0's one-shot
     call (nothing waits on a later launch): its results are the oracle's
