@@ -30,6 +30,18 @@ MUTANTS = {
     "row_stride_wrong": ("const int64_t base = i * H;", "const int64_t base = i * (H - 1);"),
     "truncating_round": ("nearbyint(ldexp(ax, -qexp))", "trunc(ldexp(ax, -qexp))"),
     "ties_away": ("nearbyint(ldexp(ax, -qexp))", "round(ldexp(ax, -qexp))"),
+    "one_stage_also_rounds": ("if (two_stage)\n        acc =", "if (1)\n        acc ="),
+    "first_rank_dropped": ("float acc = oracle_bf16_to_f32(partials[0][idx]);",
+                           "float acc = 0.0f;"),
+    "eps_dropped": ("1.0 / sqrt(ss / (double)H + eps)", "1.0 / sqrt(ss / (double)H)"),
+    "square_sum_of_rounded_residual": (
+        "ss += (double)r * (double)r;",
+        "{ double q = oracle_bf16_to_f32(residual_out[base + j]); ss += q * q; }"),
+    "output_from_rounded_residual": (
+        "double y = (double)r_scratch[j] * inv",
+        "double y = (double)oracle_bf16_to_f32(residual_out[base + j]) * inv"),
+    "weight_ignored": ("* (double)oracle_bf16_to_f32(weight[j]);", "* 1.0;"),
+    "mean_over_h_minus_one": ("ss / (double)H + eps", "ss / (double)(H - 1) + eps"),
 }
 
 
