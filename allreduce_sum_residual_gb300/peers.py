@@ -21,6 +21,10 @@ separate GPUs with ``ar_barrier`` on signal pads mapped the same way, or,
 for ranks sharing one GPU, on the host (stream synchronisation and a
 process-group barrier), since kernels of ranks on one GPU must never wait
 on one another.
+
+``FusedAllReduceRMSNorm`` puts it together for a tensor-parallel group:
+setup (buffers, mapping, collective decline) once, then one call per layer
+that picks the one-shot or the two-shot path by the number of rows.
 """
 from typing import Callable, List, Optional, Sequence
 
@@ -60,6 +64,10 @@ def map_peer_buffers(tensors: Sequence, group=None,
         get_handle = get_handle or ar_ipc_get_handle
         open_handle = open_handle or ar_ipc_open
         close_handle = close_handle or ar_ipc_close
+    if not (dist.is_available() and dist.is_initialized()):
+        # one process, no group: every buffer is this rank's own
+        return PeerMap([[int(t.data_ptr()) if hasattr(t, "data_ptr") else int(t)]
+                        for t in tensors], [], close_handle)
     rank = dist.get_rank(group)
     world = dist.get_world_size(group)
     ok = True
@@ -132,4 +140,106 @@ def ar_reduce_scatter_store_peers(partials: Sequence[int], temps: Sequence[int],
     _check(st, "ar_reduce_scatter_store")
 
 
-__all__ = ["PeerMap", "map_peer_buffers", "ar_rmsnorm_peers", "ar_reduce_scatter_store_peers"]
+def one_shot_max_rows(world: int) -> int:
+    """Rows up to which a tensor-parallel group of ``world`` ranks takes the
+    one-shot path (every rank reads every rank's partial) rather than the
+    two-shot path: 32 up to 4 ranks and 16 from 8, the rule ROCm/aiter #3817
+    keeps for MI355X across GPUs (Test Results, thresholds from #3458); 5 to
+    7 ranks take the 8-rank value.  No measurement across GB300s backs it
+    yet; one would replace it."""
+    return 32 if world <= 4 else 16
+
+
+class FusedAllReduceRMSNorm:
+    """The fused all-reduce + residual + RMSNorm of one tensor-parallel group.
+
+    ``create`` (every rank, once, outside graph capture) allocates this
+    rank's buffers -- the partial that the layer writes its output into
+    (``partial(m)``), two temporaries for the two-shot path and a signal pad
+    -- and maps every rank's copies (``map_peer_buffers``), or returns None
+    on every rank when any rank failed (tokenspeed #968's collective
+    fallback).  A call then runs, on the caller's stream, the one-shot path
+    (``ar_rmsnorm_one_shot``: barrier, epilogue, barrier) up to
+    ``one_shot_rows`` rows and the two-shot path (``ar_rmsnorm_two_shot``)
+    above, with epochs from the signal pads.  Every rank must make the same
+    sequence of calls.
+
+    Two-shot calls alternate between the two temporaries: a faster rank's
+    next stage 1 may store into a temporary that a slower rank's stage 2 is
+    still reading.  A CUDA graph fixes the alternation it captured, so a
+    graph that is replayed back to back must capture an even number of
+    two-shot calls, or end with ``barrier()``.
+    """
+
+    def __init__(self, pm, partial, own, rank, world, one_shot_rows):
+        self._pm = pm
+        self._partial = partial          # this rank's [max_rows, H] partial
+        self._own = own                  # this rank's tensors, kept alive while mapped
+        self.rank, self.world = rank, world
+        self.max_rows, self.hidden = partial.shape
+        self.one_shot_rows = one_shot_rows
+        self.two_shot_calls = 0
+
+    @classmethod
+    def create(cls, max_rows: int, hidden: int, group=None, device=None,
+               one_shot_rows: Optional[int] = None, map_buffers: Optional[Callable] = None):
+        """Set up on every rank of ``group``; None on every rank if any failed."""
+        import torch
+        import torch.distributed as dist
+        from . import AR_SIGNAL_PAD_BYTES
+        if max_rows < 1 or hidden < 8 or hidden % 8:
+            raise ValueError("max_rows >= 1 and hidden a positive multiple of 8 are required")
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+            torch.device(device)
+        partial = torch.zeros((max_rows, hidden), dtype=torch.bfloat16, device=dev)
+        temps = [torch.zeros((max_rows, hidden), dtype=torch.bfloat16, device=dev)
+                 for _ in range(2)]
+        pad = torch.zeros(AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device=dev)
+        pm = (map_buffers or map_peer_buffers)([partial, temps[0], temps[1], pad], group=group)
+        if pm is None:
+            return None
+        on = dist.is_available() and dist.is_initialized()
+        rank = dist.get_rank(group) if on else 0
+        world = dist.get_world_size(group) if on else 1
+        rows = one_shot_max_rows(world) if one_shot_rows is None else int(one_shot_rows)
+        return cls(pm, partial, (temps, pad), rank, world, rows)
+
+    def partial(self, m: int):
+        """This rank's partial for an m-row call: the [m, H] tensor the layer
+        writes its output into before the call."""
+        if not 0 <= m <= self.max_rows:
+            raise ValueError(f"m = {m} is outside 0 .. {self.max_rows}")
+        return self._partial[:m]
+
+    def path(self, m: int) -> str:
+        return "one_shot" if m <= self.one_shot_rows else "two_shot"
+
+    def __call__(self, residual, weight, eps, out=None, residual_out=None, stream=None):
+        """out, residual_out for this rank, from every rank's partial(m)."""
+        from . import ar_rmsnorm_one_shot, ar_rmsnorm_two_shot
+        m = residual.shape[0]
+        if m > self.max_rows or residual.shape[1] != self.hidden:
+            raise ValueError(f"residual {tuple(residual.shape)} does not fit "
+                             f"[<= {self.max_rows}, {self.hidden}]")
+        partials, pads = self._pm[0], self._pm[3]
+        if self.path(m) == "one_shot":
+            return ar_rmsnorm_one_shot(partials, residual, weight, eps, pads, self.rank, out=out,
+                                       residual_out=residual_out, stream=stream)
+        temps = self._pm[1 + self.two_shot_calls % 2]
+        self.two_shot_calls += 1
+        return ar_rmsnorm_two_shot(partials, residual, weight, eps, temps, pads, self.rank,
+                                   out=out, residual_out=residual_out, stream=stream)
+
+    def barrier(self, limit_us: int = 1000000, stream=None):
+        """A barrier of the group on the signal pads (the next epoch)."""
+        from . import ar_barrier
+        ar_barrier(self._pm[3], self.rank, limit_us=limit_us, stream=stream)
+
+    def close(self):
+        """Unmap the other ranks' buffers, after every call has completed on
+        every rank."""
+        self._pm.close()
+
+
+__all__ = ["PeerMap", "map_peer_buffers", "ar_rmsnorm_peers", "ar_reduce_scatter_store_peers",
+           "one_shot_max_rows", "FusedAllReduceRMSNorm"]

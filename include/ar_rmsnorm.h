@@ -410,6 +410,14 @@ int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned 
  * device's memory.  Arguments otherwise as ar_rmsnorm and
  * ar_reduce_scatter_store; no temp may overlap a partial, another temp or an
  * output (AR_ERR_ALIAS).
+ * Reuse across calls.  After the barrier no rank reads a partial any more,
+ * so each rank may overwrite its own partial once its call is issued.  The
+ * temporaries are different: rank r's stage 2 reads temps[r] after the
+ * barrier, while a faster rank's next stage 1 may already store into it.
+ * Consecutive calls must therefore alternate between two sets of
+ * temporaries (a set is written again only after every rank has passed the
+ * next call's barrier, which follows its own stage 2 of the call before),
+ * or put an ar_barrier between the calls.
  */
 int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual,
                         const void *weight, float eps, int64_t m, int64_t H, void *out,

@@ -192,3 +192,93 @@ def test_peer_mapping_is_collective(fail_rank, fail_at):
         assert got[1] == (1, [[0, 1000], [1 + 16, 1001]], 2)
     else:
         assert got == [(0, None, 0), (1, None, 0)]
+
+
+def _tp_group_rank(rank, world, port, fail_rank, q):
+    """One gloo rank setting up FusedAllReduceRMSNorm on CPU tensors with fake
+    IPC handles, then making a sequence of calls whose library entry points
+    are replaced by recorders: which path each call takes and which
+    buffers it passes."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch
+    import torch.distributed as dist
+    import allreduce_sum_residual_gb300 as arn
+    from allreduce_sum_residual_gb300 import peers
+    dist.init_process_group("gloo")
+
+    def fake_map(tensors, group=None):
+        index = {id(t): i for i, t in enumerate(tensors)}
+
+        def get_handle(t):
+            if rank == fail_rank:
+                raise RuntimeError("IPC handle failure injected on this rank")
+            return bytes([rank, index[id(t)]]) + bytes(62), 0
+
+        return peers.map_peer_buffers(tensors, group, get_handle=get_handle,
+                                      open_handle=lambda h, off: 1000 * (1 + h[0]) + h[1],
+                                      close_handle=lambda h: None)
+
+    g = peers.FusedAllReduceRMSNorm.create(64, 1024, device="cpu", map_buffers=fake_map)
+    dist.barrier()
+    if g is None:
+        q.put((rank, None))
+        dist.destroy_process_group()
+        return
+    calls = []
+    arn.ar_rmsnorm_one_shot = lambda p, res, w, eps, pads, r, **kw: calls.append(
+        ("one_shot", res.shape[0], list(p), list(pads), r))
+    arn.ar_rmsnorm_two_shot = lambda p, res, w, eps, temps, pads, r, **kw: calls.append(
+        ("two_shot", res.shape[0], list(temps), r))
+    w = torch.ones(1024, dtype=torch.bfloat16)
+    for m in (8, 40, 40, 32, 33, 64):
+        g(torch.zeros((m, 1024), dtype=torch.bfloat16), w, 1e-6)
+    bad = []
+    for m in (65, 0):
+        try:
+            g.partial(m)
+        except ValueError:
+            bad.append(m)
+    q.put((rank, (g.rank, g.world, g.one_shot_rows, tuple(g.partial(5).shape), calls, bad)))
+    g.close()
+    dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("fail_rank", [None, 1])
+def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
+    """FusedAllReduceRMSNorm on two gloo ranks: one-shot up to 32 rows
+    (2 ranks), two-shot above with the two temporaries in turn, the other
+    rank's buffers in rank order; or, when one rank's setup fails, None on
+    both."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_tp_group_rank, args=(r, 2, port, fail_rank, q))
+             for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    if fail_rank is not None:
+        assert got == [(0, None), (1, None)]
+        return
+    for rank, (r, world, rows, shape, calls, bad) in got:
+        assert (r, world, rows, shape, bad) == (rank, 2, 32, (5, 1024), [65])
+        assert [c[:2] for c in calls] == [("one_shot", 8), ("two_shot", 40), ("two_shot", 40),
+                                          ("one_shot", 32), ("two_shot", 33), ("two_shot", 64)]
+        peer = 1 - rank
+
+        def addr(i):   # buffer i of both ranks, in rank order, as this rank sees them
+            row = [None, None]
+            row[peer] = 1000 * (1 + peer) + i
+            return row
+
+        one = [c for c in calls if c[0] == "one_shot"]
+        two = [c for c in calls if c[0] == "two_shot"]
+        for c in one:
+            assert c[2][peer] == addr(0)[peer] and c[3][peer] == addr(3)[peer] and c[4] == rank
+        temps_peer = [c[2][peer] for c in two]
+        assert temps_peer == [addr(1)[peer], addr(2)[peer], addr(1)[peer], addr(2)[peer]]

@@ -298,6 +298,65 @@ def test_one_shot_replays_from_a_cuda_graph_with_fresh_epochs():
             assert int(p[arn.AR_MAX_RANKS]) == 2 * (replay + 2)
 
 
+def test_tp_group_object_on_one_rank():
+    """FusedAllReduceRMSNorm without a process group (one rank): the layer
+    writes into partial(m), then one-shot calls (m <= 32) and two-shot calls
+    (alternating temporaries) each give the oracle's result, with automatic
+    epochs, eagerly and replayed from a CUDA graph."""
+    from allreduce_sum_residual_gb300 import peers
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    H = 4096
+    g = peers.FusedAllReduceRMSNorm.create(256, H)
+    assert g is not None and (g.rank, g.world, g.one_shot_rows) == (0, 1, 32)
+    for m, seed in ((8, 1), (100, 2), (100, 3), (32, 4), (256, 5)):
+        w = synth.Workload("tp_group", n=1, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=seed)
+        inp = device_inputs(w, m)
+        g.partial(m).copy_(inp.partials[0])
+        out, rout = g(inp.residual, inp.weight, inp.eps)
+        torch.cuda.synchronize()
+        assert arn.ar_device_status(0, reset=True) == arn.AR_OK, m
+        compare((out, rout, None), oracle_rows(inp, None, g.path(m) == "two_shot"),
+                f"tp group m={m} {g.path(m)}")
+    assert g.two_shot_calls == 3
+    # two calls (one-shot, two-shot) captured once and replayed on new inputs
+    stream = torch.cuda.Stream()
+    ins = [device_inputs(synth.Workload("tp_graph", n=1, H=H, ms=(m,), p_std=0.5, res_std=1.0,
+                                       seed=10 + m), m) for m in (16, 64)]
+    outs = [(torch.empty_like(i.residual), torch.empty_like(i.residual)) for i in ins]
+
+    def step():
+        for i, (o, r) in zip(ins, outs):
+            g.partial(i.residual.shape[0]).copy_(i.partials[0])
+            g(i.residual, i.weight, i.eps, out=o, residual_out=r, stream=stream)
+        g.barrier(stream=stream)
+
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for replay in range(2):
+        for k, i in enumerate(ins):
+            fresh = device_inputs(synth.Workload("tp_graph", n=1, H=H, ms=(i.residual.shape[0],),
+                                                 p_std=0.5, res_std=1.0, seed=50 + 2 * replay + k),
+                                  i.residual.shape[0])
+            i.partials[0].copy_(fresh.partials[0])
+            i.residual.copy_(fresh.residual)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            graph.replay()
+        torch.cuda.synchronize()
+        assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+        for i, (o, r) in zip(ins, outs):
+            m = i.residual.shape[0]
+            compare((o, r, None), oracle_rows(i, None, g.path(m) == "two_shot"),
+                    f"tp group graph replay {replay} m={m}")
+    g.close()
+
+
 # ---------------------------------------------------------------- two processes, CUDA IPC
 
 def _free_port():
