@@ -38,13 +38,18 @@
  * pack = 8 bf16).
  *
  * Ownership: all tensors belong to the caller and live in device memory of
- * the current device.  The library owns only the two-stage workspace, and
- * only after ar_reserve_workspace.  The host array `partials` is read during
- * the call only and may be freed when the call returns.
+ * the current device (ar_rmsnorm_mapped and the cross-rank calls also take
+ * host, IPC and peer mappings).  The library owns only the two-stage
+ * workspace, after ar_reserve_workspace, and the fixed scratch array of
+ * ar_rmsnorm_two_stage_static.  The host pointer arrays (`partials`,
+ * `temps`, `pads`) are read during the call only and may be freed when the
+ * call returns.
  *
  * Streams: every call is asynchronous on `stream` (a cudaStream_t; NULL is
- * the legacy default stream).  No call that launches work synchronises the
- * host or allocates, so the calls may be captured in a CUDA graph.  The
+ * the legacy default stream).  No call of the compute path -- the epilogue
+ * calls, the stage calls, the signal, barrier, one-shot and two-shot calls
+ * -- synchronises the host or allocates, so they may be captured in a CUDA
+ * graph (setup and self-test calls may do both).  The
  * first launching call on a device sets kernel attributes and reads the
  * kernels' occupancy for the launch plan; make one call (or
  * ar_reserve_workspace) before capturing.
