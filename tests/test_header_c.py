@@ -48,3 +48,22 @@ def test_c_program_links_and_calls_the_library(arlib, tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr)
+
+
+@pytest.mark.skipif(shutil.which("g++") is None, reason="needs g++")
+def test_header_compiles_as_cpp_and_links_with_c_linkage(arlib, tmp_path):
+    """The same program as C++17 (extern "C" in the header): the symbols
+    resolve unmangled."""
+    src = tmp_path / "use_ar.cpp"
+    src.write_text(C_PROGRAM.replace("memset(&plan, 0, sizeof plan);",
+                                     "std::memset(&plan, 0, sizeof plan);")
+                   .replace("#include <string.h>", "#include <cstring>"))
+    exe = tmp_path / "use_ar_cpp"
+    libdir = os.path.dirname(arlib.LIB_PATH)
+    r = subprocess.run(["g++", "-std=c++17", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                        f"-I{os.path.join(ROOT, 'include')}", str(src), "-o", str(exe),
+                        f"-L{libdir}", "-l:libarnorm.so", f"-Wl,-rpath,{libdir}"],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), (r.returncode, r.stdout, r.stderr)
