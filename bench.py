@@ -437,8 +437,10 @@ def rank_latency(arn, inps, eps, stream, calls, replays, kind):
     slice into the n temporaries, then runs stage 2 on its temporary (the
     other slices of its output are not those of this call).  "one_shot":
     ar_rmsnorm_one_shot -- barrier, the epilogue over all n partials,
-    barrier.  The single-rank critical path of each cross-rank path (a
-    timing comparator).  Same method as graph_latency."""
+    barrier; "one_shot_no_end_barrier" -- the same without the second
+    barrier, as a group alternating between two partial buffers runs it.
+    The single-rank critical path of each cross-rank path (a timing
+    comparator).  Same method as graph_latency."""
     import torch
     n = len(inps[0].partials)
     like = inps[0].residual
@@ -455,7 +457,7 @@ def rank_latency(arn, inps, eps, stream, calls, replays, kind):
                                     residual_out=r)
         else:
             arn.ar_rmsnorm_one_shot(i.partials, i.residual, i.weight, eps, pads, 0, out=o,
-                                    residual_out=r)
+                                    residual_out=r, end_barrier=kind == "one_shot")
 
     def call(c):
         one(inps[c % len(inps)], *outs[c % len(outs)])
@@ -487,7 +489,7 @@ def latency_table(arn, synth, stream, l2_bytes, quick):
                 cold_t = graph_latency(arn, cold, mode, w.eps, stream, calls, replays)
                 entry[mode] = {"us_hot": round(hot * 1e6, 3), "us_cold": round(cold_t * 1e6, 3),
                                "gbs_cold": round(set_bytes / cold_t / 1e9, 1)}
-            for kind in ("two_shot", "one_shot"):
+            for kind in ("two_shot", "one_shot", "one_shot_no_end_barrier"):
                 hot = rank_latency(arn, [base], w.eps, stream, calls, replays, kind)
                 cold_t = rank_latency(arn, cold, w.eps, stream, calls, replays, kind)
                 entry[kind + "_one_rank"] = {"us_hot": round(hot * 1e6, 3),

@@ -228,11 +228,13 @@ def _tp_group_rank(rank, world, port, fail_rank, q):
         return
     calls = []
     arn.ar_rmsnorm_one_shot = lambda p, res, w, eps, pads, r, **kw: calls.append(
-        ("one_shot", res.shape[0], list(p), list(pads), r))
+        ("one_shot", res.shape[0], list(p), list(pads), r, kw.get("end_barrier", True)))
     arn.ar_rmsnorm_two_shot = lambda p, res, w, eps, temps, pads, r, **kw: calls.append(
-        ("two_shot", res.shape[0], list(temps), r))
+        ("two_shot", res.shape[0], list(p), list(temps), r))
     w = torch.ones(1024, dtype=torch.bfloat16)
+    written = []
     for m in (8, 40, 40, 32, 33, 64):
+        written.append(g.partial(m).data_ptr())      # the buffer this call reads as this rank's
         g(torch.zeros((m, 1024), dtype=torch.bfloat16), w, 1e-6)
     bad = []
     for m in (65, 0):
@@ -240,7 +242,9 @@ def _tp_group_rank(rank, world, port, fail_rank, q):
             g.partial(m)
         except ValueError:
             bad.append(m)
-    q.put((rank, (g.rank, g.world, g.one_shot_rows, tuple(g.partial(5).shape), calls, bad)))
+    own = [c[2][rank] for c in calls]
+    q.put((rank, (g.rank, g.world, g.one_shot_rows, tuple(g.partial(5).shape), calls, bad,
+                  written == own)))
     g.close()
     dist.destroy_process_group()
 
@@ -248,9 +252,10 @@ def _tp_group_rank(rank, world, port, fail_rank, q):
 @pytest.mark.parametrize("fail_rank", [None, 1])
 def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
     """FusedAllReduceRMSNorm on two gloo ranks: one-shot up to 32 rows
-    (2 ranks), two-shot above with the two temporaries in turn, the other
-    rank's buffers in rank order; or, when one rank's setup fails, None on
-    both."""
+    (2 ranks) without an end barrier, two-shot above; the two partials in
+    turn call by call (partial(m) hands out the one the next call reads),
+    the two temporaries in turn over the two-shot calls, the other rank's
+    buffers in rank order; or, when one rank's setup fails, None on both."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = free_port()
@@ -265,20 +270,18 @@ def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
     if fail_rank is not None:
         assert got == [(0, None), (1, None)]
         return
-    for rank, (r, world, rows, shape, calls, bad) in got:
-        assert (r, world, rows, shape, bad) == (rank, 2, 32, (5, 1024), [65])
+    for rank, (r, world, rows, shape, calls, bad, own_partial_ok) in got:
+        assert (r, world, rows, shape, bad, own_partial_ok) == (rank, 2, 32, (5, 1024), [65],
+                                                                True)
         assert [c[:2] for c in calls] == [("one_shot", 8), ("two_shot", 40), ("two_shot", 40),
                                           ("one_shot", 32), ("two_shot", 33), ("two_shot", 64)]
         peer = 1 - rank
-
-        def addr(i):   # buffer i of both ranks, in rank order, as this rank sees them
-            row = [None, None]
-            row[peer] = 1000 * (1 + peer) + i
-            return row
-
-        one = [c for c in calls if c[0] == "one_shot"]
-        two = [c for c in calls if c[0] == "two_shot"]
-        for c in one:
-            assert c[2][peer] == addr(0)[peer] and c[3][peer] == addr(3)[peer] and c[4] == rank
-        temps_peer = [c[2][peer] for c in two]
-        assert temps_peer == [addr(1)[peer], addr(2)[peer], addr(1)[peer], addr(2)[peer]]
+        addr = lambda i: 1000 * (1 + peer) + i     # the peer's buffer i, as this rank sees it
+        # buffers 0 and 1: the partials, alternating call by call
+        assert [c[2][peer] for c in calls] == [addr(0), addr(1)] * 3
+        for c in calls:
+            if c[0] == "one_shot":        # the pads, this rank, and no end barrier
+                assert c[3][peer] == addr(4) and c[4] == rank and c[5] is False
+            else:                         # buffers 2 and 3: the temporaries, alternating
+                assert c[4] == rank
+        assert [c[3][peer] for c in calls if c[0] == "two_shot"] == [addr(2), addr(3)] * 2
