@@ -208,6 +208,29 @@ class FusedAllReduceRMSNorm:
         rows = one_shot_max_rows(world) if one_shot_rows is None else int(one_shot_rows)
         return cls(pm, bufs[:2], (bufs[2:], pad), rank, world, rows)
 
+    _cache = {}                          # key -> group object, or _DECLINED
+    _DECLINED = object()
+
+    @classmethod
+    def for_group(cls, max_rows: int, hidden: int, group=None, device=None,
+                  one_shot_rows: Optional[int] = None, map_buffers: Optional[Callable] = None):
+        """``create`` once per (group, max_rows, hidden, device), then the same
+        object -- or, after a decline, None without trying again: the
+        permanent decline tokenspeed #968's review asks for (a setup that
+        failed is not retried on every call, so no rank takes the collective
+        setup path alone).  Every rank must call it with the same arguments
+        in the same order, as for ``create``."""
+        import torch
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
+            torch.device(device)
+        key = (id(group), max_rows, hidden, str(dev), one_shot_rows)
+        hit = cls._cache.get(key)
+        if hit is None:
+            made = cls.create(max_rows, hidden, group=group, device=dev,
+                              one_shot_rows=one_shot_rows, map_buffers=map_buffers)
+            hit = cls._cache[key] = made if made is not None else cls._DECLINED
+        return None if hit is cls._DECLINED else hit
+
     def partial(self, m: int):
         """This rank's partial for the next call, with m rows: the [m, H]
         tensor the layer writes its output into before that call."""

@@ -285,3 +285,51 @@ def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
             else:                         # buffers 2 and 3: the temporaries, alternating
                 assert c[4] == rank
         assert [c[3][peer] for c in calls if c[0] == "two_shot"] == [addr(2), addr(3)] * 2
+
+
+def _tp_cache_rank(rank, world, port, q):
+    """One gloo rank asking for the group object three times: the first ask
+    fails on rank 1 (both decline), the later asks return None at once on
+    both ranks without another setup; another size sets up afresh."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+    from allreduce_sum_residual_gb300 import peers
+    dist.init_process_group("gloo")
+    setups = []
+
+    def fake_map(tensors, group=None, fail=False):
+        setups.append(len(tensors))
+        index = {id(t): i for i, t in enumerate(tensors)}
+
+        def get_handle(t):
+            if fail and rank == 1:
+                raise RuntimeError("IPC handle failure injected on this rank")
+            return bytes([rank, index[id(t)]]) + bytes(62), 0
+
+        return peers.map_peer_buffers(tensors, group, get_handle=get_handle,
+                                      open_handle=lambda h, off: 1000 * (1 + h[0]) + h[1],
+                                      close_handle=lambda h: None)
+
+    F = peers.FusedAllReduceRMSNorm
+    failing = lambda t, group=None: fake_map(t, group, fail=True)
+    a = [F.for_group(32, 1024, device="cpu", map_buffers=failing) for _ in range(3)]
+    b = [F.for_group(64, 1024, device="cpu", map_buffers=fake_map) for _ in range(2)]
+    q.put((rank, [x is None for x in a], b[0] is not None and b[0] is b[1], setups))
+    dist.destroy_process_group()
+
+
+def test_tp_group_decline_is_kept():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = free_port()
+    procs = [ctx.Process(target=_tp_cache_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    got = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # one setup for the declined size, one for the other, on both ranks
+    assert got == [(0, [True, True, True], True, [5, 5]), (1, [True, True, True], True, [5, 5])]
