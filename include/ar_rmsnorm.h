@@ -112,7 +112,10 @@ extern "C" {
  *   residual_out [m, H] bf16, device: bf16(sum + residual); may be residual.
  *   mode         AR_MODE_AUTO, AR_MODE_ONE_STAGE or AR_MODE_TWO_STAGE.
  *   stream       cudaStream_t to launch on.
- * Returns AR_OK or an AR_ERR_* code; on error nothing is launched.
+ * Returns AR_OK or an AR_ERR_* code.  Argument errors are found before
+ * anything is launched.  A call of several launches (two-stage; the one-
+ * and two-shot calls) that gets AR_ERR_CUDA from a later launch leaves the
+ * earlier ones enqueued; the stream's results are then undefined.
  */
 int ar_rmsnorm(const void *const *partials, int n, const void *residual,
                const void *weight, float eps, int64_t m, int64_t H, void *out,
