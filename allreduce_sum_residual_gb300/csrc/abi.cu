@@ -297,10 +297,10 @@ cudaError_t launch_stream(const void *const *inputs, int n, const void *residual
   return cudaGetLastError();
 }
 
-void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n,
-                               const void *residual, const void *weight, float eps, int64_t m,
-                               int64_t H, void *out, void *residual_out, float *sum_out,
-                               const ar_plan_t &pl, int *status) {
+void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n, const void *residual,
+                        const void *weight, float eps, int64_t m, int64_t H, void *out,
+                        void *residual_out, float *sum_out, const ar_plan_t &pl,
+                        const DeviceState &d) {
   std::memset(a, 0, sizeof *a);
   for (int k = 0; k < n; ++k) a->p[k] = static_cast<const uint4 *>(inputs[k]);
   a->res = static_cast<const uint4 *>(residual);
@@ -314,21 +314,11 @@ void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n,
   a->H = static_cast<float>(H);
   a->eps = eps;
   a->wait_limit_ns = kWaitLimitNs;
-  a->status = status;
+  a->status = d.status;
   a->prefetch_own = pl.prefetch == AR_PREFETCH_ROW || pl.prefetch == AR_PREFETCH_ROW_AHEAD;
-  a->ahead = 0;
-  if (pl.prefetch == AR_PREFETCH_ROW_AHEAD) {
-    int sms = 0;
-    const DeviceState *d = nullptr;
-    int dev = -1;
-    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices && g_dev[dev].ready) {
-      d = &g_dev[dev];
-      sms = d->sms;
-    } else {
-      cudaGetLastError();
-    }
-    if (d != nullptr) a->ahead = resident_rows(pl, n, sms, device_register_occupancy);
-  }
+  a->ahead = pl.prefetch == AR_PREFETCH_ROW_AHEAD
+                 ? resident_rows(pl, n, d.sms, device_register_occupancy)
+                 : 0;
 }
 
 // True if the current device `dev` can use `p` at the same address: its own
@@ -407,7 +397,7 @@ static int run(const void *const *partials, int n, const void *residual, const v
     } else {
       EpilogueArgs a;
       fill_epilogue_args(&a, inputs, count, residual, weight, eps, m, H, out, residual_out,
-                         sum_out, pl, d->status);
+                         sum_out, pl, *d);
       e = launch_epilogue(a, count, pl, after_prior, s);
     }
     return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
@@ -486,7 +476,7 @@ int two_stage_with_temp(const void *const *partials, int n, const void *residual
   } else {
     EpilogueArgs a;
     fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
-                       d->status);
+                       *d);
     e = launch_epilogue(a, 1, pl, true, s);
   }
   return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;

@@ -65,9 +65,12 @@ int make_plan(int n, int64_t m, int64_t H, int mode, int sms, int smem_optin,
               bool plain_loads = false);
 
 // --- launches (abi.cu, reduce_flat.cu)
+// The epilogue kernel's arguments for a plan on device `d` (its status
+// word; its SM count sets the prefetch distance one wave ahead).
 void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n, const void *residual,
                         const void *weight, float eps, int64_t m, int64_t H, void *out,
-                        void *residual_out, float *sum_out, const ar_plan_t &pl, int *status);
+                        void *residual_out, float *sum_out, const ar_plan_t &pl,
+                        const DeviceState &d);
 cudaError_t launch_epilogue(const EpilogueArgs &a, int n, const ar_plan_t &pl, bool after_prior,
                             cudaStream_t stream);
 cudaError_t launch_stream(const void *const *inputs, int n, const void *residual,

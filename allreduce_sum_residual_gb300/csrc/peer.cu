@@ -435,7 +435,7 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
   } else {
     EpilogueArgs a;
     fill_epilogue_args(&a, temp_in, 1, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
-                       d->status);
+                       *d);
     e = launch_epilogue(a, 1, pl, true, s);
   }
   return e == cudaSuccess ? AR_OK : AR_ERR_CUDA;
@@ -472,7 +472,7 @@ int ar_rmsnorm_one_shot(const void *const *partials, int n, const void *residual
   // before its wait and the partials after it.
   EpilogueArgs a;
   fill_epilogue_args(&a, partials, n, residual, weight, eps, m, H, out, residual_out, nullptr, pl,
-                     d->status);
+                     *d);
   if (launch_epilogue(a, n, pl, true, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return AR_ERR_CUDA;
   if (!end_barrier) return AR_OK;
