@@ -16,8 +16,8 @@ namespace arn {
 // One-stage up to this many rows, two-stage above.  Measured on GB300 with
 // both paths at n in {4, 8}, H in {4096, 8192}, m = 1 .. 16384 (the bench's
 // sweep mode, cold buffers, graphs of back-to-back calls): one-stage was
-// faster at every point -- by 1.6-2.4 us at m <= 64 (two-stage adds a launch)
-// and by 1.25-1.7x at m >= 512 (two-stage moves (n+5)/(n+3) of the bytes).
+// faster at every point -- by 1.1-1.6 us at m <= 64 (two-stage adds a launch)
+// and by 1.09-1.42x at m >= 512 (two-stage moves (n+5)/(n+3) of the bytes).
 // On one GPU there is no cross-GPU traffic for the two-stage reduce-scatter
 // to save, so the threshold is unbounded for every (n, H).  (The pages' rule,
 // one-stage for m <= 32 at 4 ranks and m <= 16 at 8, was set on MI355X
