@@ -300,6 +300,12 @@ static int check_pads(void *const *pads, int world, int rank) {
   return AR_OK;
 }
 
+// The epoch of a call's second barrier: e + 1 (1 where that wraps to 0), or
+// AR_EPOCH_AUTO again, which takes the next value of the pad's counter.
+static uint32_t next_epoch(uint32_t e) {
+  return e == AR_EPOCH_AUTO ? AR_EPOCH_AUTO : (e + 1u == 0u ? 1u : e + 1u);
+}
+
 static int signal_call(void *const *pads, const void *mine, int world, int rank, uint32_t epoch,
                        unsigned limit_us, bool post, bool wait, void *stream) {
   if (wait && (limit_us == 0 || limit_us > 10000000u)) return AR_ERR_ARG;
@@ -404,6 +410,9 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
                  device_register_occupancy);
   if (st != AR_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  // Every rank's partial is written: stage 1 reads a slice of each.
+  st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+  if (st != AR_OK) return st;
   // Stage 1: this rank's slice, stored into every rank's temporary.  The
   // partials and temporaries of other ranks are peer mappings: no bulk
   // prefetch there.
@@ -424,7 +433,7 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
     if (launch_reduce_flat(ra, n, d->sms, s) != cudaSuccess) return AR_ERR_CUDA;
   }
   // Every rank's stores into this rank's temporary have landed.
-  st = signal_call(pads, pads[rank], world, rank, epoch, limit_us, true, true, stream);
+  st = signal_call(pads, pads[rank], world, rank, next_epoch(epoch), limit_us, true, true, stream);
   if (st != AR_OK) return st;
   // Stage 2 on this rank's (local) temporary.
   const void *temp_in[1] = {temps[rank]};
@@ -477,9 +486,8 @@ int ar_rmsnorm_one_shot(const void *const *partials, int n, const void *residual
     return AR_ERR_CUDA;
   if (!end_barrier) return AR_OK;
   // No rank reads a partial any more: each may overwrite its own.
-  const uint32_t next =
-      epoch == AR_EPOCH_AUTO ? AR_EPOCH_AUTO : (epoch + 1u == 0u ? 1u : epoch + 1u);
-  return signal_call(pads, pads[rank], world, rank, next, limit_us, true, true, stream);
+  return signal_call(pads, pads[rank], world, rank, next_epoch(epoch), limit_us, true, true,
+                     stream);
 }
 
 }  // extern "C"

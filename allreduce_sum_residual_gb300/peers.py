@@ -155,35 +155,33 @@ class FusedAllReduceRMSNorm:
 
     ``create`` (every rank, once, outside graph capture) allocates this
     rank's buffers -- two partials that the layer writes its output into
-    (``partial(m)``), two temporaries for the two-shot path and a signal pad
-    -- and maps every rank's copies (``map_peer_buffers``), or returns None
-    on every rank when any rank failed (tokenspeed #968's collective
+    (``partial(m)``), a temporary for the two-shot path and a signal pad --
+    and maps every rank's copies (``map_peer_buffers``), or returns None on
+    every rank when any rank failed (tokenspeed #968's collective
     fallback).  A call then runs, on the caller's stream, the one-shot path
     (``ar_rmsnorm_one_shot``: barrier, epilogue) up to ``one_shot_rows``
-    rows and the two-shot path (``ar_rmsnorm_two_shot``) above, with epochs
-    from the signal pads.  Every rank must make the same sequence of calls.
+    rows and the two-shot path (``ar_rmsnorm_two_shot``: barrier, stage 1,
+    barrier, stage 2) above, with epochs from the signal pads.  Every rank
+    must make the same sequence of calls.
 
-    Why two of each.  Calls alternate between the two partials, so the
-    one-shot path needs no second barrier: a rank writes a partial again
-    two calls later, after it has passed the barrier of the call in
-    between, which every rank reaches only once it has finished reading
-    that partial.  Two-shot calls alternate between the two temporaries
-    for the same reason: a faster rank's next stage 1 may store into the
-    temporary that a slower rank's stage 2 is still reading.  A CUDA graph
-    fixes the alternation it captured, so a graph that is replayed back to
-    back must capture an even number of calls and of two-shot calls, or end
+    Why two partials.  Calls alternate between them, so the one-shot path
+    needs no second barrier: a rank writes a partial again two calls
+    later, after it has passed the first barrier of the call in between,
+    which every rank reaches only once it has finished reading that
+    partial.  (The two-shot path's own barriers make one temporary enough.)
+    A CUDA graph fixes the alternation it captured, so a graph that is
+    replayed back to back must capture an even number of calls, or end
     with ``barrier()``.
     """
 
     def __init__(self, pm, partials, own, rank, world, one_shot_rows):
-        self._pm = pm                    # 0, 1: partials; 2, 3: temporaries; 4: signal pads
+        self._pm = pm                    # 0, 1: partials; 2: temporaries; 3: signal pads
         self._partials = partials        # this rank's two [max_rows, H] partials
         self._own = own                  # this rank's other tensors, kept alive while mapped
         self.rank, self.world = rank, world
         self.max_rows, self.hidden = partials[0].shape
         self.one_shot_rows = one_shot_rows
         self.calls = 0
-        self.two_shot_calls = 0
 
     @classmethod
     def create(cls, max_rows: int, hidden: int, group=None, device=None,
@@ -197,7 +195,7 @@ class FusedAllReduceRMSNorm:
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else \
             torch.device(device)
         bufs = [torch.zeros((max_rows, hidden), dtype=torch.bfloat16, device=dev)
-                for _ in range(4)]
+                for _ in range(3)]
         pad = torch.zeros(AR_SIGNAL_PAD_BYTES // 4, dtype=torch.int32, device=dev)
         pm = (map_buffers or map_peer_buffers)(bufs + [pad], group=group)
         if pm is None:
@@ -248,21 +246,19 @@ class FusedAllReduceRMSNorm:
         if m > self.max_rows or residual.shape[1] != self.hidden:
             raise ValueError(f"residual {tuple(residual.shape)} does not fit "
                              f"[<= {self.max_rows}, {self.hidden}]")
-        partials, pads = self._pm[self.calls % 2], self._pm[4]
+        partials, pads = self._pm[self.calls % 2], self._pm[3]
         self.calls += 1
         if self.path(m) == "one_shot":
             return ar_rmsnorm_one_shot(partials, residual, weight, eps, pads, self.rank, out=out,
                                        residual_out=residual_out, end_barrier=False,
                                        stream=stream)
-        temps = self._pm[2 + self.two_shot_calls % 2]
-        self.two_shot_calls += 1
-        return ar_rmsnorm_two_shot(partials, residual, weight, eps, temps, pads, self.rank,
+        return ar_rmsnorm_two_shot(partials, residual, weight, eps, self._pm[2], pads, self.rank,
                                    out=out, residual_out=residual_out, stream=stream)
 
     def barrier(self, limit_us: int = 1000000, stream=None):
         """A barrier of the group on the signal pads (the next epoch)."""
         from . import ar_barrier
-        ar_barrier(self._pm[4], self.rank, limit_us=limit_us, stream=stream)
+        ar_barrier(self._pm[3], self.rank, limit_us=limit_us, stream=stream)
 
     def close(self):
         """Unmap the other ranks' buffers, after every call has completed on

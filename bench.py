@@ -395,11 +395,12 @@ def allgather_two_stage_us(arn, inp, stream, calls=20, replays=5):
 
 def two_shot_all_ranks_us(arn, inp, stream, calls=20, replays=5):
     """The cross-rank two-shot path with every rank on this GPU, run in turn
-    so that no kernel waits on a later launch: ranks 1 .. n-1 store their
-    stage-1 slice into all n temporaries and post their flag, then rank 0's
-    ar_rmsnorm_two_shot (its slice, the barrier -- which finds every flag
-    set -- and stage 2).  Epochs come from the signal pads, so the graph
-    replays with fresh ones.  Returns (per-call µs, status word after)."""
+    so that no kernel waits on a later launch: ranks 1 .. n-1 post their
+    flag, store their stage-1 slice into all n temporaries and post again,
+    then rank 0's ar_rmsnorm_two_shot (barrier, its slice, barrier -- both
+    find every flag set -- and stage 2).  Epochs come from the signal pads,
+    so the graph replays with fresh ones.  Returns (per-call µs, status
+    word after)."""
     import torch
     n = len(inp.partials)
     temps = [torch.empty_like(inp.residual) for _ in range(n)]
@@ -410,6 +411,7 @@ def two_shot_all_ranks_us(arn, inp, stream, calls=20, replays=5):
 
     def call(c):
         for r in range(1, n):
+            arn.ar_signal_post(pads, r)
             arn.ar_reduce_scatter_store(inp.partials, temps, r)
             arn.ar_signal_post(pads, r)
         arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps, pads, 0,
@@ -433,9 +435,10 @@ def rank_latency(arn, inps, eps, stream, calls, replays, kind):
     """Per-call time of one rank's cross-rank call (rank 0 of n = the number
     of partials) when every peer is already there: the peers' flags in every
     pad are set far ahead of rank 0's epochs, so its barriers never wait.
-    `kind` "two_shot": ar_rmsnorm_two_shot -- rank 0 reduces only its own
-    slice into the n temporaries, then runs stage 2 on its temporary (the
-    other slices of its output are not those of this call).  "one_shot":
+    `kind` "two_shot": ar_rmsnorm_two_shot -- a barrier, rank 0 reduces
+    only its own slice into the n temporaries, a barrier, then stage 2 on
+    its temporary (the other slices of its output are not those of this
+    call).  "one_shot":
     ar_rmsnorm_one_shot -- barrier, the epilogue over all n partials,
     barrier; "one_shot_no_end_barrier" -- the same without the second
     barrier, as a group alternating between two partial buffers runs it.
@@ -841,8 +844,9 @@ def run_ours(args):
                     "us": round(t_ts, 2), "gbs": round(bytes_step / t_ts / 1e3, 1),
                     "gbs_actual_bytes": round(ag_bytes / t_ts / 1e3, 1),
                     "status": arn.ar_strerror(ts_status),
-                    "note": "ar_rmsnorm_two_shot of rank 0 after ranks 1..n-1 ran their stage 1 "
-                            "and posted: slices into n temporaries, flag barrier, stage 2"}
+                    "note": "ar_rmsnorm_two_shot of rank 0 after ranks 1..n-1 posted, ran their "
+                            "stage 1 and posted again: flag barrier, slices into n temporaries, "
+                            "flag barrier, stage 2"}
                 t_os = rank_latency(arn, [inp], inp.eps, stream, 20, 5, "one_shot") * 1e6
                 modes["one_shot_one_rank"] = {
                     "us": round(t_os, 2), "gbs": round(bytes_step / t_os / 1e3, 1),

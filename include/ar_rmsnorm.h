@@ -407,25 +407,28 @@ int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned 
 
 /*
  * Two-stage epilogue of rank `rank` of `world` ranks, all on `stream`:
- * stage 1 reduces this rank's slice of the packs (as ar_reduce_scatter_store)
- * across the n partials and stores it into every rank's temporary
- * temps[0 .. world-1]; ar_barrier(pads, world, rank, epoch, limit_us); then
+ * ar_barrier(pads, world, rank, epoch, limit_us), after which every rank's
+ * partial is written; stage 1, which reduces this rank's slice of the
+ * packs (as ar_reduce_scatter_store) across the n partials and stores it
+ * into every rank's temporary temps[0 .. world-1]; a second barrier, after
+ * which every rank's stores into this rank's temporary have landed; then
  * stage 2 (residual add and RMSNorm) on temps[rank], this rank's own.  The
  * results equal ar_rmsnorm's two-stage results once every rank has run it
- * with the same epoch (ROCm/aiter #3817, Technical Details, 2stage, across
- * processes).  partials[k] and temps[d] of other ranks are peer or
- * IPC mappings; temps[rank], residual, weight, out and residual_out are this
- * device's memory.  Arguments otherwise as ar_rmsnorm and
- * ar_reduce_scatter_store; no temp may overlap a partial, another temp or an
- * output (AR_ERR_ALIAS).
- * Reuse across calls.  After the barrier no rank reads a partial any more,
- * so each rank may overwrite its own partial once its call is issued.  The
- * temporaries are different: rank r's stage 2 reads temps[r] after the
- * barrier, while a faster rank's next stage 1 may already store into it.
- * Consecutive calls must therefore alternate between two sets of
- * temporaries (a set is written again only after every rank has passed the
- * next call's barrier, which follows its own stage 2 of the call before),
- * or put an ar_barrier between the calls.
+ * with the same epochs (ROCm/aiter #3817, Technical Details, 2stage, across
+ * processes: stage 1 reads a slice of every rank's partial and stores into
+ * every rank's temporary, so both barriers are needed).
+ *   epoch   an explicit epoch e: the second barrier uses e + 1 (1 if that
+ *           wraps to 0), so the next call passes e + 2.  AR_EPOCH_AUTO
+ *           takes both from the pad's counter.
+ * partials[k] and temps[d] of other ranks are peer or IPC mappings;
+ * temps[rank], residual, weight, out and residual_out are this device's
+ * memory.  Arguments otherwise as ar_rmsnorm and ar_reduce_scatter_store;
+ * no temp may overlap a partial, another temp or an output (AR_ERR_ALIAS).
+ * Reuse across calls: one partial and one set of temporaries serve every
+ * call.  A rank's next writes into its partial follow its second barrier,
+ * which every rank passes only after its stage 1 read the partials; a
+ * rank's next stage 1 stores into the temporaries only after the next
+ * call's first barrier, which every rank passes only after its stage 2.
  */
 int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual,
                         const void *weight, float eps, int64_t m, int64_t H, void *out,

@@ -254,8 +254,8 @@ def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
     """FusedAllReduceRMSNorm on two gloo ranks: one-shot up to 32 rows
     (2 ranks) without an end barrier, two-shot above; the two partials in
     turn call by call (partial(m) hands out the one the next call reads),
-    the two temporaries in turn over the two-shot calls, the other rank's
-    buffers in rank order; or, when one rank's setup fails, None on both."""
+    the other rank's buffers in rank order; or, when one rank's setup
+    fails, None on both."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = free_port()
@@ -281,10 +281,9 @@ def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
         assert [c[2][peer] for c in calls] == [addr(0), addr(1)] * 3
         for c in calls:
             if c[0] == "one_shot":        # the pads, this rank, and no end barrier
-                assert c[3][peer] == addr(4) and c[4] == rank and c[5] is False
-            else:                         # buffers 2 and 3: the temporaries, alternating
-                assert c[4] == rank
-        assert [c[3][peer] for c in calls if c[0] == "two_shot"] == [addr(2), addr(3)] * 2
+                assert c[3][peer] == addr(3) and c[4] == rank and c[5] is False
+            else:                         # buffer 2: the temporaries, every time
+                assert c[3][peer] == addr(2) and c[4] == rank
 
 
 def _tp_cache_rank(rank, world, port, q):
@@ -332,4 +331,4 @@ def test_tp_group_decline_is_kept():
         p.join(timeout=60)
         assert p.exitcode == 0
     # one setup for the declined size, one for the other, on both ranks
-    assert got == [(0, [True, True, True], True, [5, 5]), (1, [True, True, True], True, [5, 5])]
+    assert got == [(0, [True, True, True], True, [4, 4]), (1, [True, True, True], True, [4, 4])]

@@ -132,8 +132,9 @@ def test_one_and_two_shot_calls_pass_their_checks(checklib):
     assert checklib.ar_device_status(0, 1) == arn.AR_OK
     compare((out, rout, None), oracle_rows(inp, None, False), "checking build, one-shot")
     for r in range(1, world):
-        assert checklib.ar_reduce_scatter_store(arr, world, m * H, r, world, tarr, None) == arn.AR_OK
         assert checklib.ar_signal_post(parr, world, r, 3, None) == arn.AR_OK
+        assert checklib.ar_reduce_scatter_store(arr, world, m * H, r, world, tarr, None) == arn.AR_OK
+        assert checklib.ar_signal_post(parr, world, r, 4, None) == arn.AR_OK
     assert checklib.ar_rmsnorm_two_shot(arr, world, *args, tarr, parr, 3, 1_000_000,
                                         None) == arn.AR_OK
     torch.cuda.synchronize()

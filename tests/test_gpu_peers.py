@@ -121,9 +121,10 @@ def test_all_ranks_of_a_barrier_in_one_cooperative_kernel(world):
 @pytest.mark.parametrize("world,m,H", [(1, 64, 4096), (2, 77, 4104), (4, 300, 7168),
                                        (8, 16, 6144), (3, 5, 24)])
 def test_two_shot_with_the_other_ranks_run_first(world, m, H):
-    """Ranks 1 .. world-1 run their stage 1 and post before rank 0's whole
-    two-shot call: its barrier finds every flag set (nothing waits on a
-    later launch), and its results are the two-stage results."""
+    """Ranks 1 .. world-1 post the first epoch, run their stage 1 and post
+    the second before rank 0's whole two-shot call: both its barriers find
+    every flag set (nothing waits on a later launch), and its results are
+    the two-stage results."""
     torch.cuda.set_device(0)
     arn.ar_device_status(0, reset=True)
     w = synth.Workload("two_shot", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=world + m)
@@ -131,8 +132,9 @@ def test_two_shot_with_the_other_ranks_run_first(world, m, H):
     temps = [torch.zeros((m, H), dtype=torch.bfloat16, device="cuda") for _ in range(world)]
     pads = _pads(world)
     for r in range(1, world):
+        arn.ar_signal_post(pads, r, 1)                 # its partial is written
         arn.ar_reduce_scatter_store(inp.partials, temps, r)
-        arn.ar_signal_post(pads, r, 1)
+        arn.ar_signal_post(pads, r, 2)                 # its stores have landed
     out, rout = arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps,
                                         pads, 0, 1)
     if arn.ar_workspace_elems(0) < m * H:
@@ -149,10 +151,10 @@ def test_two_shot_with_the_other_ranks_run_first(world, m, H):
 
 
 def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
-    """The emulated ranks' calls (the other ranks' stage 1 and posts, then
-    rank 0's two-shot call), captured once in a CUDA graph with automatic
-    epochs and replayed on new inputs: every replay synchronises on a new
-    epoch and matches the oracle."""
+    """The emulated ranks' calls (the other ranks' two posts around their
+    stage 1, then rank 0's two-shot call), captured once in a CUDA graph
+    with automatic epochs and replayed on new inputs: every replay
+    synchronises on two new epochs and matches the oracle."""
     torch.cuda.set_device(0)
     arn.ar_device_status(0, reset=True)
     world, m, H = 4, 48, 2056
@@ -166,6 +168,7 @@ def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
 
     def call():
         for r in range(1, world):
+            arn.ar_signal_post(pads, r, stream=stream)
             arn.ar_reduce_scatter_store(inp.partials, temps, r, stream=stream)
             arn.ar_signal_post(pads, r, stream=stream)
         arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps, pads, 0,
@@ -173,12 +176,12 @@ def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
 
     torch.cuda.synchronize()
     with torch.cuda.stream(stream):
-        call()                                         # eager: epoch 1
+        call()                                         # eager: epochs 1 and 2
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         call()
-    for replay in range(3):                            # epochs 2, 3, 4
+    for replay in range(3):                            # epochs 3-4, 5-6, 7-8
         fresh = device_inputs(synth.Workload("two_shot_graph", n=world, H=H, ms=(m,), p_std=0.5,
                                              res_std=1.0, seed=100 + replay), m)
         for dst, src in zip(inp.partials + [inp.residual], fresh.partials + [fresh.residual]):
@@ -190,7 +193,7 @@ def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
         assert arn.ar_device_status(0, reset=True) == arn.AR_OK, replay
         compare((out, rout, temps[0].float()), oracle_rows(inp, None, True), f"replay {replay}")
         for p in pads:
-            assert int(p[arn.AR_MAX_RANKS]) == replay + 2
+            assert int(p[arn.AR_MAX_RANKS]) == 2 * (replay + 2)
 
 
 def _mapped_one_stage(inp):
@@ -301,8 +304,8 @@ def test_one_shot_replays_from_a_cuda_graph_with_fresh_epochs():
 def test_tp_group_object_on_one_rank():
     """FusedAllReduceRMSNorm without a process group (one rank): the layer
     writes into partial(m), then one-shot calls (m <= 32) and two-shot calls
-    (alternating temporaries) each give the oracle's result, with automatic
-    epochs, eagerly and replayed from a CUDA graph."""
+    each give the oracle's result, with automatic epochs, eagerly and
+    replayed from a CUDA graph."""
     from allreduce_sum_residual_gb300 import peers
     torch.cuda.set_device(0)
     arn.ar_device_status(0, reset=True)
@@ -318,7 +321,7 @@ def test_tp_group_object_on_one_rank():
         assert arn.ar_device_status(0, reset=True) == arn.AR_OK, m
         compare((out, rout, None), oracle_rows(inp, None, g.path(m) == "two_shot"),
                 f"tp group m={m} {g.path(m)}")
-    assert g.two_shot_calls == 3
+    assert g.calls == 5
     # two calls (one-shot, two-shot) captured once and replayed on new inputs
     stream = torch.cuda.Stream()
     ins = [device_inputs(synth.Workload("tp_graph", n=1, H=H, ms=(m,), p_std=0.5, res_std=1.0,
