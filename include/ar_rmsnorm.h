@@ -293,7 +293,9 @@ int ar_reduce_scatter_flat(const void *const *partials, int n, int64_t count,
  * Technical Details, 2stage, reduce-scatter: each reduced pack is stored
  * straight into the temporary of every rank).  Once all `world`
  * ranks have run it, and synchronised, every temp holds the whole bf16 sum
- * and stage 2 (ar_load_rmsnorm) can run on any of them.
+ * and stage 2 (ar_load_rmsnorm) can run on any of them.  Across processes
+ * the ranks must also synchronise before it, since it reads a slice of
+ * every rank's partial (ar_rmsnorm_two_shot does both).
  *   partials  host array of n device pointers, count bf16 each.
  *   temps     host array of `world` device pointers, count bf16 each; on
  *             one GPU local buffers (the n-copy write of the all-gather is
