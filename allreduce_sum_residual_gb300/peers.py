@@ -16,11 +16,12 @@ The returned ``PeerMap`` gives, per buffer, the device addresses of all
 ranks' copies in rank order, ready for the peer-pointer calls
 ``ar_rmsnorm_peers`` (one-shot: every rank reads every rank's partial) and
 ``ar_reduce_scatter_store_peers`` (stage 1 of the two-shot path: stores into
-every rank's temporary).  Between the stages the ranks synchronise: on
-separate GPUs with ``ar_barrier`` on signal pads mapped the same way, or,
-for ranks sharing one GPU, on the host (stream synchronisation and a
-process-group barrier), since kernels of ranks on one GPU must never wait
-on one another.
+every rank's temporary).  Before stage 1 (or the one-shot epilogue) and
+between the stages the ranks synchronise: on separate GPUs with
+``ar_barrier`` on signal pads mapped the same way (``ar_rmsnorm_one_shot``
+and ``ar_rmsnorm_two_shot`` do it themselves), or, for ranks sharing one
+GPU, on the host (stream synchronisation and a process-group barrier),
+since kernels of ranks on one GPU must never wait on one another.
 
 ``FusedAllReduceRMSNorm`` puts it together for a tensor-parallel group:
 setup (buffers, mapping, collective decline) once, then one call per layer
