@@ -16,7 +16,9 @@ What it checks is the argument the library's documentation makes:
 * the two-shot call, with a barrier before stage 1 and one between the
   stages, is safe with one partial and one set of temporaries; without the
   first barrier a fast rank's stage 1 reads a partial its owner is still
-  writing.
+  writing;
+* a CUDA graph of the group object's calls, replayed back to back, needs
+  an even number of captured calls or a barrier at its end.
 """
 import random
 
@@ -140,3 +142,33 @@ def test_the_group_objects_mixed_calls_are_safe(world):
              "two_shot"]
     assert _races(world, len(kinds), kinds, partial_sets=2, temp_sets=1) == 0
     assert _races(world, len(kinds), kinds, partial_sets=1, temp_sets=1) > 0
+
+
+def _replayed_one_shots(world, captured, replays, barrier_at_end):
+    """The group object's one-shot calls captured once in a CUDA graph and
+    replayed: the partial of each captured call is fixed at capture, so
+    `captured` calls use partials 0, 1, 0, ... again on every replay."""
+    progs = []
+    for r in range(world):
+        ev, k = [], 0
+        for _ in range(replays):
+            for i in range(captured):
+                ev += _one_shot(r, world, k, i % 2, end_barrier=False)
+                k += 1
+            if barrier_at_end:
+                ev += [("post", ("graph_end", k)), ("wait", ("graph_end", k))]
+        progs.append(ev)
+    return progs
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_a_replayed_graph_needs_an_even_number_of_calls_or_a_final_barrier(world):
+    rng = random.Random(1)
+
+    def races(captured, barrier_at_end):
+        progs = _replayed_one_shots(world, captured, 4, barrier_at_end)
+        return sum(_run(progs, rng) is not None for _ in range(300))
+
+    assert races(2, False) == 0 and races(4, False) == 0
+    assert races(3, False) > 0          # the replay boundary reuses a partial back to back
+    assert races(3, True) == 0
