@@ -5,9 +5,10 @@
   kernels on the stream let it pass; epochs compare modulo 2^32.
 * All ranks of a barrier inside one cooperative kernel (they run at the same
   time), checking that data written before a post is seen after the wait.
-* The two-shot path (stage 1 stored into every rank's temporary, barrier,
-  stage 2) with the other ranks' parts run earlier on the stream, so that
-  no kernel waits on a later one: against the oracle's two-stage result.
+* The two-shot path (barrier, stage 1 stored into every rank's temporary,
+  barrier, stage 2) with the other ranks' parts run earlier on the stream,
+  so that no kernel waits on a later one: against the oracle's two-stage
+  result.
 * The one-shot call (barrier, epilogue over every rank's partial, barrier)
   with the other ranks' posts run earlier: against the oracle's one-stage
   result; a rank that never reaches the end barrier; graph replay.
