@@ -361,8 +361,11 @@ int ar_rmsnorm_two_stage_static(const void *const *partials, int n,
  *
  * ROCm/aiter #3817, Technical Details, 2stage, reduce-scatter: each rank
  * reduces its slice of the packs across every rank's partial and stores the
- * bf16 sums straight into every rank's temporary, so every rank's stores
- * must have landed before any rank's stage 2 reads its own temporary.
+ * bf16 sums straight into every rank's temporary, so every rank's partial
+ * must be written before any rank's stage 1 reads it, and every rank's
+ * stores must have landed before any rank's stage 2 reads its own
+ * temporary; in the 1stage path every rank reads every rank's partial,
+ * which must be written first.
  * lightseekorg/tokenspeed #968, Summary: the ranks' buffers are mapped into
  * each other's address spaces through IPC handles, with a collective
  * fallback when that setup fails on any rank.
@@ -403,7 +406,8 @@ int ar_signal_post(void *const *pads, int world, int rank, uint32_t epoch, void 
 int ar_signal_wait(const void *pad, int world, uint32_t epoch, unsigned limit_us, void *stream);
 
 /* Post, then wait on pads[rank]: a barrier of the `world` ranks (the same
-   passages as ar_signal_post). */
+   passages as ar_signal_post).  The posting rank does not wait on its own
+   flag, which it has just stored. */
 int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned limit_us,
                void *stream);
 
