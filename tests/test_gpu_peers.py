@@ -151,6 +151,35 @@ def test_two_shot_with_the_other_ranks_run_first(world, m, H):
     assert torch.equal(rout.view(torch.int16), ref_rout.view(torch.int16))
 
 
+@pytest.mark.parametrize("kind", ["one_shot", "two_shot"])
+def test_an_explicit_epoch_at_the_wrap_takes_one_next(kind):
+    """A call given epoch 2^32 - 1 runs its second barrier on epoch 1 (0 is
+    the automatic-epoch value): the other ranks post those two epochs and
+    rank 0's call passes both barriers."""
+    torch.cuda.set_device(0)
+    arn.ar_device_status(0, reset=True)
+    world, m, H = 2, 8, 1024
+    w = synth.Workload("wrap", n=world, H=H, ms=(m,), p_std=0.5, res_std=1.0)
+    inp = device_inputs(w, m)
+    pads = _pads(world)
+    temps = [torch.zeros((m, H), dtype=torch.bfloat16, device="cuda") for _ in range(world)]
+    last = 0xFFFFFFFF
+    arn.ar_signal_post(pads, 1, last)
+    if kind == "two_shot":
+        arn.ar_reduce_scatter_store(inp.partials, temps, 1)
+    arn.ar_signal_post(pads, 1, 1)
+    if kind == "one_shot":
+        out, rout = arn.ar_rmsnorm_one_shot(inp.partials, inp.residual, inp.weight, inp.eps, pads,
+                                            0, last, limit_us=100_000)
+    else:
+        out, rout = arn.ar_rmsnorm_two_shot(inp.partials, inp.residual, inp.weight, inp.eps, temps,
+                                            pads, 0, last, limit_us=100_000)
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0, reset=True) == arn.AR_OK
+    assert _flags(pads[1], world) == [1, 1]
+    compare((out, rout, None), oracle_rows(inp, None, kind == "two_shot"), f"{kind} at the wrap")
+
+
 def test_two_shot_replays_from_a_cuda_graph_with_fresh_epochs():
     """The emulated ranks' calls (the other ranks' two posts around their
     stage 1, then rank 0's two-shot call), captured once in a CUDA graph
