@@ -250,7 +250,7 @@ def _tp_group_rank(rank, world, port, fail_rank, q):
 
 
 @pytest.mark.parametrize("fail_rank", [None, 1])
-def test_tp_group_picks_paths_and_alternates_temporaries(fail_rank):
+def test_tp_group_picks_paths_and_alternates_partials(fail_rank):
     """FusedAllReduceRMSNorm on two gloo ranks: one-shot up to 32 rows
     (2 ranks) without an end barrier, two-shot above; the two partials in
     turn call by call (partial(m) hands out the one the next call reads),
