@@ -326,7 +326,7 @@ void fill_epilogue_args(EpilogueArgs *a, const void *const *inputs, int n, const
 // (cudaHostAlloc, cudaHostRegister; with unified addressing the device
 // address equals the host address).  Pageable host memory, another device's
 // memory and unknown pointers are refused.
-static bool device_accessible(const void *p, int dev) {
+bool device_accessible(const void *p, int dev) {
   cudaPointerAttributes at;
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     cudaGetLastError();

@@ -52,6 +52,8 @@ int check_buffers(const void *const *partials, int n, const void *residual, cons
 // cannot be queried).
 int check_mapped(const void *const *partials, int n, const void *residual, const void *weight,
                  const void *out, const void *residual_out);
+// One pointer of check_mapped's kinds, for device `dev`.
+bool device_accessible(const void *p, int dev);
 
 // --- the launch plan (plan.cu)
 int select_mode(int n, int64_t m, int64_t H);

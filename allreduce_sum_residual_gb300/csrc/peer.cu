@@ -403,6 +403,16 @@ int ar_rmsnorm_two_shot(const void *const *partials, int n, const void *residual
   if (overlap(mine, range_of(out, bytes)) || overlap(mine, range_of(residual_out, bytes)) ||
       overlap(mine, range_of(residual, bytes)) || overlap(mine, range_of(weight, H * 2)))
     return AR_ERR_ALIAS;
+  // Every pointer reachable from this device (its own, IPC or peer memory).
+  st = check_mapped(partials, n, residual, weight, out, residual_out);
+  if (st != AR_OK) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return AR_ERR_CUDA;
+  }
+  for (int e = 0; e < world; ++e)
+    if (!device_accessible(temps[e], dev)) return AR_ERR_ARG;
   DeviceState *d = current_device(&st);
   if (!d) return st;
   ar_plan_t pl;

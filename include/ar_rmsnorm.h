@@ -428,8 +428,10 @@ int ar_barrier(void *const *pads, int world, int rank, uint32_t epoch, unsigned 
  *           takes both from the pad's counter.
  * partials[k] and temps[d] of other ranks are peer or IPC mappings;
  * temps[rank], residual, weight, out and residual_out are this device's
- * memory.  Arguments otherwise as ar_rmsnorm and ar_reduce_scatter_store;
- * no temp may overlap a partial, another temp or an output (AR_ERR_ALIAS).
+ * memory.  Every pointer is checked as ar_rmsnorm_mapped checks its own
+ * (AR_ERR_ARG for memory this device cannot reach).  Arguments otherwise
+ * as ar_rmsnorm and ar_reduce_scatter_store; no temp may overlap a
+ * partial, another temp or an output (AR_ERR_ALIAS).
  * Reuse across calls: one partial and one set of temporaries serve every
  * call.  A rank's next writes into its partial follow its second barrier,
  * which every rank passes only after its stage 1 read the partials; a
