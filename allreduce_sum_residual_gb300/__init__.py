@@ -46,6 +46,9 @@ AR_MAX_RANKS = 16
 AR_MAX_HIDDEN = 131072
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libarnorm.so")
+# The checking build (device-side bounds checks compiled in; for tests):
+# ARN_CHECK_BUILD=1 makes lib() load it instead.
+CHECK_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libarnorm_check.so")
 
 
 class ArError(RuntimeError):
@@ -142,14 +145,18 @@ def load(path):
 
 
 def lib():
-    """The loaded libarnorm.so (ctypes), with argument types set."""
+    """The loaded libarnorm.so (ctypes), with argument types set; with
+    ARN_CHECK_BUILD=1 in the environment, the checking build instead."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                f"{LIB_PATH} is not built: run `python -c \"import __graft_entry__ as g; g.build()\"`"
-                " (the CUDA library is required; there is no fallback)")
-        _lib = load(LIB_PATH)
+        checking = os.environ.get("ARN_CHECK_BUILD", "0") == "1"
+        path = CHECK_LIB_PATH if checking else LIB_PATH
+        if not os.path.exists(path):
+            how = ("python -m allreduce_sum_residual_gb300._build --check" if checking else
+                   "python -c \"import __graft_entry__ as g; g.build()\"")
+            raise RuntimeError(f"{path} is not built: run `{how}` (the CUDA library is required; "
+                               "there is no fallback)")
+        _lib = load(path)
     return _lib
 
 

@@ -566,3 +566,17 @@ def test_binding_fails_loudly_without_the_library(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
                        timeout=120)
     assert r.stdout.strip() == "raised: True", r.stdout + r.stderr
+
+
+def test_the_environment_selects_the_checking_build():
+    """ARN_CHECK_BUILD=1 makes the binding load libarnorm_check.so (bounds
+    checks compiled in), so any program or test can run against it."""
+    import subprocess
+    import sys
+    from allreduce_sum_residual_gb300 import _build
+    _build.build(check=True)
+    code = "import allreduce_sum_residual_gb300 as a; print(a.lib().ar_checks_bounds())"
+    for flag, want in (("1", "1"), ("0", "0")):
+        r = subprocess.run([sys.executable, "-c", code], cwd=ROOT, capture_output=True, text=True,
+                           timeout=300, env={**os.environ, "ARN_CHECK_BUILD": flag})
+        assert r.stdout.strip() == want, r.stdout + r.stderr
