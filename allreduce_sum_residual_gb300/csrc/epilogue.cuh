@@ -90,9 +90,10 @@ k_fused_epilogue(const __grid_constant__ EpilogueArgs a) {
 
   // Loads first: n partials, the residual and the weight of every pack this
   // thread owns.  Nothing is stored before the last load is issued.  In
-  // stage 2 the previous grid is stage 1, which writes neither the weight
-  // nor the residual (and everything before stage 1 has completed), so
-  // those two are read before the wait; the temporary only after.
+  // stage 2 the previous grid is stage 1, and in the one-shot call it is
+  // the barrier kernel; neither writes the weight or the residual (and
+  // everything before it has completed), so with early_reads those two are
+  // read before the wait, the temporary or the partials only after.
   //
   // Before that wait, lanes 0..N of warp 0 ask L2 for this CTA's slice of
   // the n partials and the residual, one bulk prefetch each.  Under
