@@ -621,3 +621,34 @@ def test_raw_c_abi_call():
     assert st == 0
     torch.cuda.synchronize()
     compare((out, rout, None), oracle_rows(inp, None, False), "raw C ABI")
+
+
+def _random_shapes(count, seed):
+    """Seeded shapes across the planner's whole range: n 1..16, H any
+    multiple of 8 up to 16384 (biased to model-like widths and to odd pack
+    counts), m 1..16 or 64..2048 with m*H kept small enough for the oracle."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    while len(shapes) < count:
+        n = int(rng.integers(1, 17))
+        H = int(rng.choice([int(rng.integers(1, 2049)) * 8,
+                            int(rng.choice([2560, 2880, 3584, 4608, 5632, 10240, 14336]))]))
+        m = int(rng.integers(1, 17)) if rng.random() < 0.3 else int(rng.integers(64, 2049))
+        if m * H <= 4_000_000:
+            shapes.append((n, m, H, str(rng.choice(["auto", "two_stage"]))))
+    return shapes
+
+
+@pytest.mark.parametrize("n,m,H,mode", _random_shapes(40, 2026))
+def test_random_shapes_against_the_oracle(n, m, H, mode):
+    """Whatever plan AUTO makes for a shape off every grid (kernel form,
+    cluster, packs per thread, prefetch), the results match the oracle."""
+    w = synth.Workload("random", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=n * 7919 + m + H)
+    inp = device_inputs(w, m)
+    if arn.ar_workspace_elems(0) < m * H:
+        arn.ar_reserve_workspace(m * H, 0)
+    out, rout, s = run_gpu(inp, mode)
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0) == arn.AR_OK
+    compare((out, rout, s), oracle_rows(inp, None, is_two_stage(n, m, H, mode)),
+            f"random n={n} m={m} H={H} {mode} plan={arn.ar_get_plan(n, m, H, mode)}")
