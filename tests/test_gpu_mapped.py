@@ -112,3 +112,33 @@ def test_empty_batch_with_host_buffers():
     out, rout = arn.ar_rmsnorm_mapped([e, e], e, wt, 1e-6)
     torch.cuda.synchronize()
     assert out.shape == (0, H) and rout.shape == (0, H)
+
+
+def _random_mapped_shapes(count, seed):
+    import numpy as np
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < count:
+        n = int(rng.integers(1, 17))
+        H = int(rng.choice([int(rng.integers(1, 1025)) * 8, 2560, 4096, 7168, 12288]))
+        m = int(rng.integers(1, 17)) if rng.random() < 0.3 else int(rng.integers(64, 1025))
+        if m * H <= 2_000_000:
+            out.append((n, m, H, str(rng.choice(["auto", "two_stage"]))))
+    return out
+
+
+@pytest.mark.parametrize("n,m,H,mode", _random_mapped_shapes(12, 7))
+def test_random_shapes_from_host_buffers(n, m, H, mode):
+    """The plain-load plans (the best register-kernel form of the table, no
+    bulk prefetch) on seeded shapes off every grid, all buffers in pinned
+    host memory: the oracle's results."""
+    w = synth.Workload("mapped_random", n=n, H=H, ms=(m,), p_std=0.5, res_std=1.0, seed=m + H + n)
+    inp = device_inputs(w, m, seed=3)
+    if arn.ar_workspace_elems(0) < m * H:
+        arn.ar_reserve_workspace(m * H, 0)
+    parts, res, wt = _host_inputs(inp, ("partials", "residual", "weight"))
+    out, rout = arn.ar_rmsnorm_mapped(parts, res, wt, inp.eps, mode=mode)
+    torch.cuda.synchronize()
+    assert arn.ar_device_status(0) == arn.AR_OK
+    compare((out, rout, None), oracle_rows(inp, None, mode == "two_stage"),
+            f"mapped random n={n} m={m} H={H} {mode}")
